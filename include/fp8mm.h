@@ -1,0 +1,161 @@
+/*
+ * fp8mm.h -- C ABI of the GB300 (sm_103a) FP8 scaled matrix multiply with a
+ * fused global amax.
+ *
+ *   C[l,m,n] = out_dtype( sum_c S_A(l,m,c) * S_B(l,n,c) * sum_{k in chunk c} A[l,m,k] * B[l,n,k] )
+ *   amax     = max over l, m, n of |C[l,m,n]|        (taken over the stored C)
+ *
+ * Sources of the operation:
+ *   - mmaemu "API reference (v0.1)", mmaemu.scaled_mm: torch._scaled_mm
+ *     semantics -- FP8 operands, one-element fp32 scales that multiply the
+ *     result, out_dtype, fast accumulation (one chain over K) or slow
+ *     accumulation (128-element chunks), prior contents of the output never
+ *     matter.
+ *   - TileOPs "Linear Algebra Operators", GemmFP8FwdOp: a is [M x K], b is
+ *     [N x K]; scales per tensor, per 1x128 block along K ([M x ceil(K/128)]),
+ *     or for b per 128x128 block ([ceil(N/128) x ceil(K/128)]).
+ *   - cuDNN "GEMM + Amax (SM100)", Shapes / Equations / Using JAX arrays:
+ *     A (M,K,L) and B (N,K,L) K-major, scale factors per sf_vec_size = 32
+ *     elements along K in the atom layout, C (M,N,L) N-major, Amax (1,1,1)
+ *     fp32 = max |C|; A, B, C 16-byte aligned along the contiguous dimension;
+ *     A and B of the same dtype for the block-scaled form.
+ *
+ * Memory layout (all row-major, batch outermost):
+ *   a        [L][M][K] FP8 codes (1 byte each), K contiguous.
+ *   b        [L][N][K] FP8 codes, K contiguous.
+ *   c        [L][M][N] of out_dtype, N contiguous.
+ *   amax     one fp32.
+ *   scale_a / scale_b, by scale_mode:
+ *     FP8MM_SCALE_TENSOR           one fp32 each.
+ *     FP8MM_SCALE_A1x128_B1x128    fp32 [L][M][ceil(K/128)] and [L][N][ceil(K/128)].
+ *     FP8MM_SCALE_A1x128_B128x128  fp32 [L][M][ceil(K/128)] and [L][ceil(N/128)][ceil(K/128)].
+ *     FP8MM_SCALE_MX32_UE8M0       UE8M0 bytes (code e means 2^(e-127), 0xFF is NaN),
+ *                                  [L][ceil(rows/128)][ceil(K/128)][32][4][4]: within one
+ *                                  512-byte atom, byte i32*16 + i4*4 + j4 scales row
+ *                                  i32 + 32*i4 of the 128-row block and the 32-element
+ *                                  K block j4 of the 128-element K block.
+ *
+ * Ownership: the caller owns every buffer (inputs, outputs, workspace) and
+ * every pointer above is a DEVICE pointer on the plan's device.  A plan holds
+ * host state only and may be reused for any number of calls with the same
+ * shapes; it is not thread-safe (one plan per host thread).
+ *
+ * Asynchrony: fp8mm_run only enqueues work on the given stream (amax is reset
+ * on the stream, then the kernel runs).  It never synchronises.  Outputs are
+ * valid once the stream reaches that point.
+ *
+ * Errors: every call returns an fp8mm_status; nothing throws across this ABI.
+ * Validation failures return before any CUDA call.  A device-side abort (an
+ * internal wait that exceeded its time limit) is recorded in a device word
+ * that fp8mm_device_error reads; the outputs of that call are then undefined.
+ */
+#ifndef FP8MM_H
+#define FP8MM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FP8MM_E4M3 = 0, FP8MM_E5M2 = 1 } fp8mm_fmt;
+
+typedef enum { FP8MM_OUT_F32 = 0, FP8MM_OUT_BF16 = 1, FP8MM_OUT_F16 = 2 } fp8mm_out;
+
+typedef enum {
+  FP8MM_SCALE_TENSOR = 0,
+  FP8MM_SCALE_A1x128_B1x128 = 1,
+  FP8MM_SCALE_A1x128_B128x128 = 2,
+  FP8MM_SCALE_MX32_UE8M0 = 3
+} fp8mm_scale_mode;
+
+typedef enum {
+  FP8MM_OK = 0,
+  FP8MM_ERR_INVALID = 1,     /* null pointer, negative size, value out of range    */
+  FP8MM_ERR_ALIGNMENT = 2,   /* a row or pointer is not 16-byte aligned (K % 16, N rows of C) */
+  FP8MM_ERR_UNSUPPORTED = 3, /* outside this library: mixed formats in the MX form, sizes >= 2^31 */
+  FP8MM_ERR_REJECTED = 4,    /* reserved for a torch-compatible strict mode       */
+  FP8MM_ERR_WORKSPACE = 5,   /* workspace missing or smaller than fp8mm_workspace_size */
+  FP8MM_ERR_CUDA = 6,        /* a CUDA runtime call or the launch failed           */
+  FP8MM_ERR_DEVICE = 7       /* the kernel aborted (see fp8mm_device_error)        */
+} fp8mm_status;
+
+/* Problem description.  Zero-initialise, then set the fields. */
+typedef struct {
+  int64_t M, N, K, L;  /* L = batch count (1 for a plain GEMM); M, N, L may be 0 */
+  int32_t a_fmt;       /* fp8mm_fmt of A */
+  int32_t b_fmt;       /* fp8mm_fmt of B */
+  int32_t scale_mode;  /* fp8mm_scale_mode */
+  int32_t out_dtype;   /* fp8mm_out */
+  int32_t fast_accum;  /* 1: one fp32 chain over K; 0: 128-K chunks promoted into an fp32
+                          register accumulator.  The block-scale modes always promote per
+                          128-K chunk (their scales change per chunk). */
+  int32_t splitk;      /* 0: choose; S >= 1: split K into S contiguous 128-aligned ranges */
+  int32_t swap_ab;     /* -1 or 0 in a zeroed struct means choose; 1 force on; 2 force off */
+  int32_t block_n;     /* 0: choose; else the tile width on the MMA's N side (16..256) */
+  int32_t device;      /* CUDA device ordinal the plan is for */
+  int32_t reserved[3]; /* must be 0 */
+} fp8mm_desc;
+
+typedef struct fp8mm_plan_s fp8mm_plan_t;
+
+/* What a plan chose (for reports and tests). */
+typedef struct {
+  int32_t swap_ab;      /* 1 if B plays the MMA's A operand (skinny M) */
+  int32_t block_m;      /* rows per tile on the MMA's M side (128) */
+  int32_t block_n;      /* tile width on the MMA's N side */
+  int32_t splitk;       /* K ranges per output tile */
+  int32_t stages;       /* shared-memory pipeline depth */
+  int32_t grid;         /* persistent CTAs launched */
+  int64_t units;        /* (tile, K range) work units */
+  int32_t slow;         /* 1 if 128-K chunks are promoted in registers */
+  int32_t smem_bytes;   /* dynamic shared memory per CTA */
+} fp8mm_plan_info;
+
+/* Validate desc and choose tiles, swap-AB and split-K for the device.  On
+ * success *out owns a new plan (free with fp8mm_destroy).  Reads the device's
+ * SM count; launches nothing. */
+fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out);
+
+/* Device bytes the caller must pass as workspace to fp8mm_run (0 if none).
+ * The split-K partial tiles and their arrival counters live there. */
+fp8mm_status fp8mm_workspace_size(const fp8mm_plan_t* plan, size_t* bytes);
+
+/* Enqueue one GEMM + amax on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  a, b, scale_a, scale_b, c, amax, workspace: device pointers laid
+ * out as described above.  a, b and c must be 16-byte aligned; scale pointers
+ * 4-byte aligned.  c and amax are written, never read. */
+fp8mm_status fp8mm_run(fp8mm_plan_t* plan, const void* a, const void* b, const void* scale_a,
+                       const void* scale_b, void* c, float* amax, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Algorithmic work of one call: flops = 2*M*N*K*L; bytes = A + B + scales +
+ * C + amax (split-K workspace traffic not counted). */
+fp8mm_status fp8mm_plan_roofline(const fp8mm_plan_t* plan, double* flops, double* bytes);
+
+fp8mm_status fp8mm_plan_get_info(const fp8mm_plan_t* plan, fp8mm_plan_info* info);
+
+void fp8mm_destroy(fp8mm_plan_t* plan);
+
+/* Static string naming a status code. */
+const char* fp8mm_status_string(fp8mm_status status);
+
+/* Read (and with clear != 0, reset) the device's abort word: 0 when no kernel
+ * on `device` has aborted since the last clear.  Synchronises the device. */
+fp8mm_status fp8mm_device_error(int device, uint32_t* code, int clear);
+
+/* Number of kernel launches fp8mm_run enqueues for this plan (the amax reset
+ * and, with split-K, the counter reset are stream memsets, not kernels). */
+fp8mm_status fp8mm_plan_kernel_launches(const fp8mm_plan_t* plan, int32_t* launches);
+
+/* One-shot form: plan, run, destroy.  Same arguments as fp8mm_plan + fp8mm_run. */
+fp8mm_status fp8mm_gemm(const fp8mm_desc* desc, const void* a, const void* b,
+                        const void* scale_a, const void* scale_b, void* c, float* amax,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8MM_H */

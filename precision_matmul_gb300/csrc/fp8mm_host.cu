@@ -1,0 +1,550 @@
+// fp8mm_host.cu -- the C ABI declared in include/fp8mm.h: validation, the
+// plan (tile shape, swap-AB, split-K, pipeline depth), TMA descriptor
+// encoding and the launch of the persistent kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "fp8mm.h"
+#include "fp8mm_kernel.cuh"
+
+using namespace fp8mm;
+
+struct fp8mm_plan_s {
+  fp8mm_desc d;
+  int sms = 0;
+  int max_smem = 0;
+  int swap = 0, bn = 0, splits = 1, kb_per_split = 0, num_kb = 0, stages = 0, num_acc = 2;
+  int group = 1, slow = 0, mx = 0, out_es = 4;
+  int64_t R = 0, Q = 0;
+  int tiles_r = 0, tiles_q = 0;
+  long long units = 0;
+  int grid = 0;
+  uint32_t tmem_cols = 0;
+  int x_kind = kScaleNone, y_kind = kScaleNone;
+  uint32_t off_x = 0, off_y = 0, off_sf = 0, off_out = 0, off_ys = 0, off_bar = 0;
+  uint32_t x_stage_bytes = 0, y_stage_bytes = 0, sf_stage_bytes = 0;
+  size_t smem_bytes = 0;
+  size_t ws_partials_bytes = 0, ws_counters_off = 0, ws_counters_bytes = 0, ws_bytes = 0;
+};
+
+namespace {
+
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const KParams);
+
+template <int BN, bool SLOW, bool MX>
+KernelFn kfn() {
+  return &fp8mm_kernel<BN, SLOW, MX>;
+}
+
+KernelFn select_kernel(int bn, bool slow, bool mx) {
+  if (mx) {
+    switch (bn) {
+      case 128: return slow ? kfn<128, true, true>() : kfn<128, false, true>();
+      case 256: return slow ? nullptr : kfn<256, false, true>();
+      default: return nullptr;
+    }
+  }
+  switch (bn) {
+    case 16: return slow ? kfn<16, true, false>() : kfn<16, false, false>();
+    case 32: return slow ? kfn<32, true, false>() : kfn<32, false, false>();
+    case 64: return slow ? kfn<64, true, false>() : kfn<64, false, false>();
+    case 128: return slow ? kfn<128, true, false>() : kfn<128, false, false>();
+    case 256: return slow ? nullptr : kfn<256, false, false>();
+    default: return nullptr;
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int out_size(int out_dtype) { return out_dtype == FP8MM_OUT_F32 ? 4 : 2; }
+
+// Per-device, per-kernel opt-in to large dynamic shared memory.
+cudaError_t ensure_smem_attr(KernelFn fn, int device, size_t bytes) {
+  static std::mutex mu;
+  static const void* done[64][16] = {};
+  std::lock_guard<std::mutex> lk(mu);
+  if (device >= 0 && device < 64) {
+    for (int i = 0; i < 16; ++i) {
+      if (done[device][i] == (const void*)fn) return cudaSuccess;
+    }
+  }
+  cudaError_t e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  if (device >= 0 && device < 64) {
+    for (int i = 0; i < 16; ++i) {
+      if (done[device][i] == nullptr) {
+        done[device][i] = (const void*)fn;
+        break;
+      }
+    }
+  }
+  return cudaSuccess;
+}
+
+// Shared-memory layout for a given stage count; returns total bytes.
+size_t layout(fp8mm_plan_s* P, int stages) {
+  const uint32_t x_bytes = kBlockM * kBlockK;
+  const uint32_t y_bytes = (uint32_t)P->bn * kBlockK;
+  const uint32_t sf_bytes = P->mx ? 512u * (1u + (uint32_t)(P->bn / 128)) : 0u;
+  uint32_t off = 0;
+  P->x_stage_bytes = x_bytes;
+  P->y_stage_bytes = y_bytes;
+  P->sf_stage_bytes = sf_bytes;
+  P->off_x = off;
+  off += x_bytes * stages;
+  P->off_y = off;
+  off += y_bytes * stages;
+  off = (off + 1023u) & ~1023u;
+  P->off_sf = off;
+  off += sf_bytes * stages;
+  off = (off + 1023u) & ~1023u;
+  P->off_out = off;
+  off += kEpiWarps * kStageOutBytes;
+  P->off_ys = off;
+  if (P->x_kind != kScaleNone) off += kEpiWarps * (P->bn / 2) * 4;
+  off = (off + 127u) & ~127u;
+  P->off_bar = off;
+  off += 16u * stages + 48u + 16u;  // full/empty per stage, 2+2 accumulator barriers, epilogue, drain, misc
+  off = (off + 127u) & ~127u;
+  return (size_t)off + 1024;  // slack for aligning the dynamic base to 1024
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8mm_status_string(fp8mm_status s) {
+  switch (s) {
+    case FP8MM_OK: return "ok";
+    case FP8MM_ERR_INVALID: return "invalid argument";
+    case FP8MM_ERR_ALIGNMENT: return "misaligned pointer or row (16-byte rule)";
+    case FP8MM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FP8MM_ERR_REJECTED: return "rejected combination";
+    case FP8MM_ERR_WORKSPACE: return "workspace missing or too small";
+    case FP8MM_ERR_CUDA: return "CUDA error";
+    case FP8MM_ERR_DEVICE: return "device-side abort";
+  }
+  return "unknown status";
+}
+
+fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
+  if (!desc || !out) return FP8MM_ERR_INVALID;
+  *out = nullptr;
+  const fp8mm_desc d = *desc;
+  if (d.M < 0 || d.N < 0 || d.K < 0 || d.L < 0) return FP8MM_ERR_INVALID;
+  if (d.a_fmt < 0 || d.a_fmt > 1 || d.b_fmt < 0 || d.b_fmt > 1) return FP8MM_ERR_INVALID;
+  if (d.out_dtype < 0 || d.out_dtype > 2) return FP8MM_ERR_INVALID;
+  if (d.scale_mode < 0 || d.scale_mode > 3) return FP8MM_ERR_INVALID;
+  if (d.fast_accum < 0 || d.fast_accum > 1) return FP8MM_ERR_INVALID;
+  if (d.splitk < 0 || d.swap_ab < 0 || d.swap_ab > 2 || d.device < 0) return FP8MM_ERR_INVALID;
+  if (d.reserved[0] || d.reserved[1] || d.reserved[2]) return FP8MM_ERR_INVALID;
+  if (d.block_n != 0 && d.block_n != 16 && d.block_n != 32 && d.block_n != 64 && d.block_n != 128 &&
+      d.block_n != 256)
+    return FP8MM_ERR_INVALID;
+  const int64_t lim = (int64_t)1 << 31;
+  if (d.M >= lim || d.N >= lim || d.K >= lim || d.L >= 65536) return FP8MM_ERR_UNSUPPORTED;
+  if (d.K % 16 != 0) return FP8MM_ERR_ALIGNMENT;
+  if ((d.N * out_size(d.out_dtype)) % 16 != 0) return FP8MM_ERR_ALIGNMENT;
+  const bool mx = d.scale_mode == FP8MM_SCALE_MX32_UE8M0;
+  if (mx && d.a_fmt != d.b_fmt) return FP8MM_ERR_UNSUPPORTED;
+  if (mx && d.block_n != 0 && d.block_n < 128) return FP8MM_ERR_UNSUPPORTED;
+
+  fp8mm_plan_s* P = new (std::nothrow) fp8mm_plan_s();
+  if (!P) return FP8MM_ERR_INVALID;
+  P->d = d;
+  if (cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&P->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device) != cudaSuccess) {
+    cudaGetLastError();
+    delete P;
+    return FP8MM_ERR_CUDA;
+  }
+  P->mx = mx ? 1 : 0;
+  P->out_es = out_size(d.out_dtype);
+  const bool blockwise = d.scale_mode == FP8MM_SCALE_A1x128_B1x128 || d.scale_mode == FP8MM_SCALE_A1x128_B128x128;
+  P->slow = (blockwise || !d.fast_accum) ? 1 : 0;
+
+  // Swap-AB for skinny M: the long N side then fills the 128-lane MMA M side.
+  bool swap;
+  if (d.swap_ab == 1)
+    swap = true;
+  else if (d.swap_ab == 2)
+    swap = false;
+  else
+    swap = !mx && d.M <= 256 && d.N > d.M;
+  if (mx && swap && d.M < 128) swap = false;
+  P->swap = swap ? 1 : 0;
+  P->R = swap ? d.N : d.M;
+  P->Q = swap ? d.M : d.N;
+  if (blockwise) {
+    if (!swap) {
+      P->x_kind = kScaleRow;
+      P->y_kind = d.scale_mode == FP8MM_SCALE_A1x128_B1x128 ? kScaleRow : kScaleBlock128;
+    } else {
+      P->x_kind = d.scale_mode == FP8MM_SCALE_A1x128_B1x128 ? kScaleRow : kScaleBlock128;
+      P->y_kind = kScaleRow;
+    }
+  }
+  P->num_kb = (int)cdiv(d.K, kBlockK);
+  const int64_t tiles_r = std::max<int64_t>(1, cdiv(P->R, kBlockM));
+
+  // Tile width on the MMA's N side.
+  int bn = d.block_n;
+  if (bn == 0) {
+    const int64_t q16 = std::max<int64_t>(16, cdiv(P->Q, 16) * 16);
+    bn = 16;
+    while (bn < q16 && bn < 256) bn *= 2;
+    if (mx && bn < 128) bn = 128;
+    // Skinny (swapped) problems are bound by streaming X from HBM: split the
+    // Y side in two when that turns 1-2 waves of tiles into ~3.
+    if (swap && bn == 256 && tiles_r * 2 <= 3 * (int64_t)P->sms) bn = 128;
+    // Slow accumulation keeps BN/2 fp32 sums per epilogue thread in registers;
+    // the MX form double-buffers its TMEM accumulator next to the factor ring.
+    if ((P->slow || mx) && bn > 128) bn = 128;
+  } else if (P->slow && bn > 128) {
+    delete P;
+    return FP8MM_ERR_UNSUPPORTED;
+  }
+  P->bn = bn;
+  const int64_t tiles_q = std::max<int64_t>(1, cdiv(P->Q, bn));
+  P->tiles_r = (int)tiles_r;
+  P->tiles_q = (int)tiles_q;
+  const int64_t tiles = tiles_r * tiles_q * std::max<int64_t>(1, d.L);
+
+  // Split-K: contiguous 128-aligned K ranges.  Chosen to fill whole waves of
+  // SMs when there are fewer than two waves of tiles and the partial tiles
+  // are small next to the operand bytes they save.
+  int S = d.splitk;
+  if (S == 0) {
+    S = 1;
+    if (tiles < 2 * (int64_t)P->sms && P->num_kb >= 8) {
+      double best = (double)tiles / (double)(cdiv(tiles, P->sms) * P->sms);
+      for (int s = 2; s <= 8; ++s) {
+        if (P->num_kb / s < 4) break;
+        if (bn > 128 && s > 2) break;
+        const int64_t u = tiles * s;
+        const double eff = (double)u / (double)(cdiv(u, P->sms) * P->sms);
+        if (eff > best + 0.05) {
+          best = eff;
+          S = s;
+        }
+      }
+    }
+  }
+  S = std::max(1, std::min(S, std::max(1, P->num_kb)));
+  P->kb_per_split = P->num_kb > 0 ? (int)cdiv(P->num_kb, S) : 0;
+  P->splits = P->num_kb > 0 ? (int)cdiv(P->num_kb, P->kb_per_split) : 1;
+  P->units = (long long)tiles * P->splits;
+  P->grid = (int)std::min<long long>(P->units, P->sms);
+  P->group = swap ? 1 : 8;
+
+  // TMEM: accumulators, then (MX) a ring of scale-factor slots of 16 columns.
+  // Pipeline depth: as many stages as fit in shared memory (at most 12).
+  int stages = 12;
+  while (stages > 2 && layout(P, stages) > (size_t)P->max_smem) --stages;
+  P->stages = stages;
+  P->smem_bytes = layout(P, stages);
+  if (P->smem_bytes > (size_t)P->max_smem) {
+    delete P;
+    return FP8MM_ERR_UNSUPPORTED;
+  }
+  const uint32_t sf_cols = mx ? 16u * (uint32_t)stages : 0u;
+  P->num_acc = (2u * bn + sf_cols <= 512u) ? 2 : 1;
+  const uint32_t need = (uint32_t)(P->num_acc * bn) + sf_cols;
+  uint32_t cols = 32;
+  while (cols < need) cols *= 2;
+  if (cols > 512) {
+    delete P;
+    return FP8MM_ERR_UNSUPPORTED;
+  }
+  P->tmem_cols = cols;
+
+  if (P->splits > 1) {
+    P->ws_partials_bytes = (size_t)tiles * P->splits * kBlockM * bn * sizeof(float);
+    P->ws_counters_off = (P->ws_partials_bytes + 255) & ~(size_t)255;
+    P->ws_counters_bytes = (size_t)tiles * sizeof(unsigned);
+    P->ws_bytes = P->ws_counters_off + ((P->ws_counters_bytes + 255) & ~(size_t)255);
+  }
+  *out = P;
+  return FP8MM_OK;
+}
+
+fp8mm_status fp8mm_workspace_size(const fp8mm_plan_t* plan, size_t* bytes) {
+  if (!plan || !bytes) return FP8MM_ERR_INVALID;
+  *bytes = plan->ws_bytes;
+  return FP8MM_OK;
+}
+
+fp8mm_status fp8mm_plan_roofline(const fp8mm_plan_t* plan, double* flops, double* bytes) {
+  if (!plan || !flops || !bytes) return FP8MM_ERR_INVALID;
+  const fp8mm_desc& d = plan->d;
+  const double L = (double)d.L, M = (double)d.M, N = (double)d.N, K = (double)d.K;
+  const double kb = (double)cdiv(d.K, 128);
+  double sbytes = 8.0;
+  switch (d.scale_mode) {
+    case FP8MM_SCALE_A1x128_B1x128: sbytes = 4.0 * L * (M + N) * kb; break;
+    case FP8MM_SCALE_A1x128_B128x128: sbytes = 4.0 * L * (M + (double)cdiv(d.N, 128)) * kb; break;
+    case FP8MM_SCALE_MX32_UE8M0:
+      sbytes = 512.0 * L * kb * (double)(cdiv(d.M, 128) + cdiv(d.N, 128));
+      break;
+    default: break;
+  }
+  *flops = 2.0 * L * M * N * K;
+  *bytes = L * (M * K + N * K) + sbytes + L * M * N * (double)plan->out_es + 4.0;
+  return FP8MM_OK;
+}
+
+fp8mm_status fp8mm_plan_get_info(const fp8mm_plan_t* plan, fp8mm_plan_info* info) {
+  if (!plan || !info) return FP8MM_ERR_INVALID;
+  info->swap_ab = plan->swap;
+  info->block_m = kBlockM;
+  info->block_n = plan->bn;
+  info->splitk = plan->splits;
+  info->stages = plan->stages;
+  info->grid = plan->grid;
+  info->units = plan->units;
+  info->slow = plan->slow;
+  info->smem_bytes = (int32_t)plan->smem_bytes;
+  return FP8MM_OK;
+}
+
+fp8mm_status fp8mm_plan_kernel_launches(const fp8mm_plan_t* plan, int32_t* launches) {
+  if (!plan || !launches) return FP8MM_ERR_INVALID;
+  const fp8mm_desc& d = plan->d;
+  *launches = (d.M == 0 || d.N == 0 || d.L == 0 || d.K == 0) ? 0 : 1;
+  return FP8MM_OK;
+}
+
+void fp8mm_destroy(fp8mm_plan_t* plan) { delete plan; }
+
+fp8mm_status fp8mm_device_error(int device, uint32_t* code, int clear) {
+  if (!code || device < 0) return FP8MM_ERR_INVALID;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return FP8MM_ERR_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return FP8MM_ERR_CUDA;
+  fp8mm_status st = FP8MM_OK;
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(&v, g_fp8mm_abort, sizeof(v)) != cudaSuccess)
+    st = FP8MM_ERR_CUDA;
+  if (st == FP8MM_OK && clear) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_fp8mm_abort, &zero, sizeof(zero)) != cudaSuccess) st = FP8MM_ERR_CUDA;
+  }
+  *code = v;
+  if (prev != device) cudaSetDevice(prev);
+  return st;
+}
+
+fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void* scale_a, const void* scale_b,
+                       void* c, float* amax, void* workspace, size_t workspace_bytes, void* stream_) {
+  if (!P || !amax) return FP8MM_ERR_INVALID;
+  const fp8mm_desc& d = P->d;
+  const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const bool empty = d.M == 0 || d.N == 0 || d.L == 0;
+  if (!empty) {
+    if (!c) return FP8MM_ERR_INVALID;
+    if (d.K > 0 && (!a || !b || !scale_a || !scale_b)) return FP8MM_ERR_INVALID;
+    if (!aligned(c, 16)) return FP8MM_ERR_ALIGNMENT;
+    if (d.K > 0) {
+      if (!aligned(a, 16) || !aligned(b, 16)) return FP8MM_ERR_ALIGNMENT;
+      const uintptr_t sal = P->mx ? 16 : 4;
+      if (!aligned(scale_a, sal) || !aligned(scale_b, sal)) return FP8MM_ERR_ALIGNMENT;
+    }
+  }
+  if (!aligned(amax, 4)) return FP8MM_ERR_ALIGNMENT;
+  if (P->ws_bytes > 0 && !empty && d.K > 0) {
+    if (!workspace || workspace_bytes < P->ws_bytes) return FP8MM_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return FP8MM_ERR_ALIGNMENT;
+  }
+
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return FP8MM_ERR_CUDA;
+  if (prev != d.device && cudaSetDevice(d.device) != cudaSuccess) return FP8MM_ERR_CUDA;
+  struct Restore {
+    int prev, dev;
+    ~Restore() {
+      if (prev != dev) cudaSetDevice(prev);
+    }
+  } restore{prev, d.device};
+
+  if (cudaMemsetAsync(amax, 0, sizeof(float), stream) != cudaSuccess) return FP8MM_ERR_CUDA;
+  if (empty) return FP8MM_OK;
+  if (d.K == 0) {
+    // An empty sum over K: every element of C is +0.
+    const size_t bytes = (size_t)d.L * d.M * d.N * P->out_es;
+    return cudaMemsetAsync(c, 0, bytes, stream) == cudaSuccess ? FP8MM_OK : FP8MM_ERR_CUDA;
+  }
+
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FP8MM_ERR_CUDA;
+  const void* xptr = P->swap ? b : a;
+  const void* yptr = P->swap ? a : b;
+  CUtensorMap tm_x, tm_y, tm_c;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)d.K, (cuuint64_t)P->R, (cuuint64_t)d.L};
+    cuuint64_t strides[2] = {(cuuint64_t)d.K, (cuuint64_t)(d.K * P->R)};
+    cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)kBlockM, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(xptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FP8MM_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)d.K, (cuuint64_t)P->Q, (cuuint64_t)d.L};
+    cuuint64_t strides[2] = {(cuuint64_t)d.K, (cuuint64_t)(d.K * P->Q)};
+    cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)P->bn, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tm_y, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(yptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FP8MM_ERR_CUDA;
+  }
+  const int half = P->bn / 2;
+  const int pw = half < 16 ? half : 16;
+  uint32_t rowbytes;
+  cuuint32_t cbox[3];
+  if (!P->swap) {
+    rowbytes = (uint32_t)(pw * P->out_es);
+    cbox[0] = (cuuint32_t)pw;
+    cbox[1] = 32;
+  } else {
+    rowbytes = (uint32_t)(32 * P->out_es);
+    cbox[0] = 32;
+    cbox[1] = (cuuint32_t)pw;
+  }
+  cbox[2] = 1;
+  CUtensorMapSwizzle cswz;
+  uint32_t swz_mask;
+  switch (rowbytes) {
+    case 128: cswz = CU_TENSOR_MAP_SWIZZLE_128B; swz_mask = 7; break;
+    case 64: cswz = CU_TENSOR_MAP_SWIZZLE_64B; swz_mask = 3; break;
+    case 32: cswz = CU_TENSOR_MAP_SWIZZLE_32B; swz_mask = 1; break;
+    default: cswz = CU_TENSOR_MAP_SWIZZLE_NONE; swz_mask = 0; break;
+  }
+  {
+    const CUtensorMapDataType dt = d.out_dtype == FP8MM_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : d.out_dtype == FP8MM_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {(cuuint64_t)d.N, (cuuint64_t)d.M, (cuuint64_t)d.L};
+    cuuint64_t strides[2] = {(cuuint64_t)(d.N * P->out_es), (cuuint64_t)(d.N * d.M * P->out_es)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tm_c, dt, 3, c, dims, strides, cbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, cswz,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FP8MM_ERR_CUDA;
+  }
+
+  KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.R = (int)P->R;
+  kp.Q = (int)P->Q;
+  kp.K = (int)d.K;
+  kp.L = (int)d.L;
+  kp.num_kb = P->num_kb;
+  kp.kb_per_split = P->kb_per_split;
+  kp.splits = P->splits;
+  kp.tiles_r = P->tiles_r;
+  kp.tiles_q = P->tiles_q;
+  kp.group = P->group;
+  kp.units = P->units;
+  kp.swap = P->swap;
+  kp.out_dtype = d.out_dtype;
+  kp.out_es = P->out_es;
+  kp.stages = P->stages;
+  kp.num_acc = P->num_acc;
+  kp.tmem_cols = P->tmem_cols;
+  const uint32_t xf = (uint32_t)(P->swap ? d.b_fmt : d.a_fmt);
+  const uint32_t yf = (uint32_t)(P->swap ? d.a_fmt : d.b_fmt);
+  if (P->mx) {
+    // kind::mxf8f6f4: B scale id bits 4-5, formats 7-9 / 10-12, N>>3 at 17, UE8M0 scale type bit 23,
+    // M>>4 at 24, A scale id bits 29-30 (ids added per K step in the kernel).
+    kp.idesc = (xf << 7) | (yf << 10) | ((uint32_t)(P->bn >> 3) << 17) | (1u << 23) |
+               ((uint32_t)(kBlockM >> 4) << 24);
+  } else {
+    // kind::f8f6f4: fp32 accumulator (bits 4-5 = 1), formats, K-major A and B, N>>3 at 17, M>>4 at 24.
+    kp.idesc = (1u << 4) | (xf << 7) | (yf << 10) | ((uint32_t)(P->bn >> 3) << 17) |
+               ((uint32_t)(kBlockM >> 4) << 24);
+  }
+  if (d.scale_mode == FP8MM_SCALE_TENSOR) {
+    kp.sa_tensor = static_cast<const float*>(scale_a);
+    kp.sb_tensor = static_cast<const float*>(scale_b);
+  } else if (P->mx) {
+    kp.sfx = static_cast<const uint8_t*>(P->swap ? scale_b : scale_a);
+    kp.sfy = static_cast<const uint8_t*>(P->swap ? scale_a : scale_b);
+  } else {
+    kp.x_scale = static_cast<const float*>(P->swap ? scale_b : scale_a);
+    kp.y_scale = static_cast<const float*>(P->swap ? scale_a : scale_b);
+    kp.x_kind = P->x_kind;
+    kp.y_kind = P->y_kind;
+  }
+  kp.scale_kb = P->num_kb;
+  kp.sfx_mb = (int)cdiv(P->R, 128);
+  kp.sfy_mb = (int)cdiv(P->Q, 128);
+  kp.sfy_atoms = P->bn / 128 > 0 ? P->bn / 128 : 1;
+  kp.amax_bits = reinterpret_cast<unsigned*>(amax);
+  if (P->splits > 1) {
+    kp.ws_partials = static_cast<float*>(workspace);
+    kp.ws_counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + P->ws_counters_off);
+    if (cudaMemsetAsync(kp.ws_counters, 0, P->ws_counters_bytes, stream) != cudaSuccess) return FP8MM_ERR_CUDA;
+  }
+  kp.off_x = P->off_x;
+  kp.off_y = P->off_y;
+  kp.off_sf = P->off_sf;
+  kp.off_out = P->off_out;
+  kp.off_ys = P->off_ys;
+  kp.off_bar = P->off_bar;
+  kp.x_stage_bytes = P->x_stage_bytes;
+  kp.y_stage_bytes = P->y_stage_bytes;
+  kp.sf_stage_bytes = P->sf_stage_bytes;
+  kp.out_swz_mask = swz_mask;
+  kp.out_rowbytes = rowbytes;
+
+  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0);
+  if (!fn) return FP8MM_ERR_UNSUPPORTED;
+  if (ensure_smem_attr(fn, d.device, P->smem_bytes) != cudaSuccess) return FP8MM_ERR_CUDA;
+  void* args[4] = {&tm_x, &tm_y, &tm_c, &kp};
+  cudaError_t e = cudaLaunchKernel((const void*)fn, dim3((unsigned)P->grid), dim3(kThreads), args, P->smem_bytes,
+                                   stream);
+  if (e != cudaSuccess) return FP8MM_ERR_CUDA;
+  return FP8MM_OK;
+}
+
+fp8mm_status fp8mm_gemm(const fp8mm_desc* desc, const void* a, const void* b, const void* scale_a,
+                        const void* scale_b, void* c, float* amax, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  fp8mm_plan_t* plan = nullptr;
+  fp8mm_status st = fp8mm_plan(desc, &plan);
+  if (st != FP8MM_OK) return st;
+  st = fp8mm_run(plan, a, b, scale_a, scale_b, c, amax, workspace, workspace_bytes, stream);
+  fp8mm_destroy(plan);
+  return st;
+}
+
+}  // extern "C"

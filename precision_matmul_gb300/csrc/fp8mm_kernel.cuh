@@ -1,0 +1,607 @@
+// fp8mm_kernel.cuh -- persistent, warp-specialised FP8 scaled GEMM + amax for
+// sm_103a.
+//
+// What one launch computes (mmaemu "API reference (v0.1)", mmaemu.scaled_mm;
+// TileOPs "Linear Algebra Operators", GemmFP8FwdOp; cuDNN "GEMM + Amax
+// (SM100)", Equations):
+//
+//   C[l,m,n] = out( sum_c S_A(l,m,c) S_B(l,n,c) sum_{k in chunk c} A[l,m,k] B[l,n,k] ),
+//   amax     = max |C|.
+//
+// The kernel works in the frame of the tensor-core instruction: X is the
+// operand on the MMA's M side (tiles of 128 rows, one TMEM lane per row) and
+// Y the operand on its N side (tiles of BN rows).  Normally X = A and Y = B;
+// for skinny M the roles swap (X = B, Y = A) and the epilogue stores the
+// tile transposed, so that the long dimension fills the 128-row side.
+//
+// Roles (320 threads, one CTA per SM, persistent over work units):
+//   warps 0-7  epilogue: TMEM -> registers; for slow accumulation and block
+//              scales, one promotion per 128-K chunk (acc += s_x s_y chunk in
+//              fp32); split-K fix-up; scale, cast, NaN canonicalisation, amax,
+//              shared-memory staging and TMA stores.
+//   warp 8     TMA producer: A/B tiles (128 B of K per row, 128-byte swizzle)
+//              and, for the MX form, the 512-byte scale-factor atoms, into a
+//              ring of `stages` shared-memory slots guarded by mbarriers.
+//   warp 9     MMA issuer: tcgen05.mma kind::f8f6f4 (or kind::mxf8f6f4 with
+//              block scaling) into one or two TMEM accumulators; also owns
+//              the TMEM allocation.
+//
+// Every wait on an mbarrier is bounded in time: when a limit is hit the
+// kernel records an error code in a device word, the other roles leave their
+// loops, in-flight copies and MMAs are drained, TMEM is freed and the kernel
+// returns.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace fp8mm {
+
+constexpr int kBlockM = 128;      // MMA M: TMEM lanes per tile
+constexpr int kBlockK = 128;      // K per pipeline stage: one 128-byte swizzle row per operand row
+constexpr int kUmmaK = 32;        // K per tcgen05.mma for 8-bit operands
+constexpr int kEpiWarps = 8;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kStageOutBytes = 2048;  // per-warp output staging buffer
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+// Abort codes (OR-ed into the device word).
+constexpr unsigned kErrProducer = 1u, kErrMmaFull = 2u, kErrMmaAcc = 4u, kErrEpiAcc = 8u,
+                   kErrEpiSync = 16u, kErrDrain = 32u;
+
+enum ScaleKind : int { kScaleNone = 0, kScaleRow = 1, kScaleBlock128 = 2 };
+
+struct KParams {
+  int R, Q, K, L;         // rows of X (MMA M side), rows of Y (MMA N side), K, batches
+  int num_kb;             // ceil(K / 128)
+  int kb_per_split;
+  int splits;
+  int tiles_r, tiles_q;
+  int group;              // tile rows per raster group
+  long long units;        // L * tiles_r * tiles_q * splits
+  int swap;               // 1: C[m][n] is tile(q = m, r = n)
+  int out_dtype;          // 0 f32, 1 bf16, 2 f16
+  int out_es;             // bytes per output element
+  int stages;
+  int num_acc;            // TMEM accumulators (1 or 2)
+  uint32_t tmem_cols;
+  uint32_t idesc;         // instruction descriptor without the scale-factor ids
+  const float* sa_tensor; // per-tensor scales (device), or null
+  const float* sb_tensor;
+  const float* x_scale;   // block scales of X and Y (fp32), or null
+  int x_kind;
+  const float* y_scale;
+  int y_kind;
+  int scale_kb;           // ceil(K / 128): row stride of the block-scale arrays and atom count along K
+  const uint8_t* sfx;     // MX scale-factor atoms of X and Y
+  const uint8_t* sfy;
+  int sfx_mb, sfy_mb;     // ceil(R / 128), ceil(Q / 128)
+  int sfy_atoms;          // atoms of Y per stage (BN / 128)
+  float* ws_partials;     // split-K partial tiles [tile][split][col][row]
+  unsigned* ws_counters;  // split-K arrivals per tile
+  unsigned* amax_bits;    // fp32 amax as its bit pattern (non-negative floats order as uints)
+  uint32_t off_x, off_y, off_sf, off_out, off_ys, off_bar;  // shared-memory layout
+  uint32_t x_stage_bytes, y_stage_bytes, sf_stage_bytes;
+  uint32_t out_swz_mask;  // 16-byte-chunk XOR mask of the output staging swizzle
+  uint32_t out_rowbytes;  // bytes per staging row
+};
+
+// Device word recording aborted waits (read by fp8mm_device_error).
+__device__ unsigned g_fp8mm_abort = 0u;
+
+struct Unit {
+  int l, tr, tq, s, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode_unit(long long u, const KParams& p) {
+  Unit t;
+  t.s = (int)(u % p.splits);
+  const long long tile = u / p.splits;
+  const long long per_l = (long long)p.tiles_r * p.tiles_q;
+  t.l = (int)(tile / per_l);
+  const long long t2 = tile - (long long)t.l * per_l;
+  const long long gspan = (long long)p.group * p.tiles_q;
+  const int grp = (int)(t2 / gspan);
+  const int first = grp * p.group;
+  const int gsize = min(p.group, p.tiles_r - first);
+  const int within = (int)(t2 - (long long)grp * gspan);
+  t.tr = first + within % gsize;
+  t.tq = within / gsize;
+  t.kb0 = t.s * p.kb_per_split;
+  t.kb1 = min(t.kb0 + p.kb_per_split, p.num_kb);
+  return t;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false if another role aborted or
+// the limit was hit (which sets the abort flag and the device error word).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         unsigned code) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1u;
+        atomicOr(&g_fp8mm_abort, code);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait used while tearing down: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(&g_fp8mm_abort, kErrDrain);
+      return;
+    }
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_load(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 32) {
+    ptx::tmem_ld_32x32b_x32(taddr, r);
+    ptx::tmem_ld_wait_x32(r);
+  } else if constexpr (N == 16) {
+    ptx::tmem_ld_32x32b_x16(taddr, r);
+    ptx::tmem_ld_wait_x16(r);
+  } else {
+    static_assert(N == 8, "tcgen05.ld width");
+    ptx::tmem_ld_32x32b_x8(taddr, r);
+    ptx::tmem_ld_wait_x8(r);
+  }
+}
+
+__device__ __forceinline__ uint32_t swz(uint32_t off, uint32_t mask) {
+  return off ^ (((off >> 7) & mask) << 4);
+}
+
+// Scales PW values of this thread's tile row, casts them to out_dtype
+// (round to nearest even; NaN becomes the canonical pattern), folds |value|
+// into the running amax (rows and columns inside C only), stages the warp's
+// 32 x PW block in shared memory and stores it with one TMA copy at (cx, cy, cl).
+template <int PW>
+__device__ __forceinline__ void store_piece(const KParams& p, const CUtensorMap* tm_c, const float (&v)[PW],
+                                            float alpha, bool row_ok, int q0, int lane, uint8_t* stg,
+                                            uint32_t stg_s, int cx, int cy, int cl, bool in_bounds,
+                                            uint32_t& amax_local) {
+  if (lane == 0) ptx::bulk_wait_read_all();  // the previous store has read the staging buffer
+  __syncwarp();
+  if (p.out_es == 4) {
+    uint32_t w[PW];
+#pragma unroll
+    for (int i = 0; i < PW; ++i) {
+      const float x = alpha * v[i];
+      uint32_t b = __float_as_uint(x);
+      uint32_t a = b & 0x7FFFFFFFu;
+      if (a > 0x7F800000u) {
+        b = 0x7FFFFFFFu;
+        a = 0x7FFFFFFFu;
+      }
+      w[i] = b;
+      if (row_ok && q0 + i < p.Q) amax_local = max(amax_local, a);
+    }
+    if (!p.swap) {
+#pragma unroll
+      for (int c = 0; c < PW / 4; ++c) {
+        const uint32_t off = swz((uint32_t)lane * p.out_rowbytes + c * 16u, p.out_swz_mask);
+        *reinterpret_cast<uint4*>(stg + off) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < PW; ++i) {
+        const uint32_t off = swz((uint32_t)i * p.out_rowbytes + lane * 4u, p.out_swz_mask);
+        *reinterpret_cast<uint32_t*>(stg + off) = w[i];
+      }
+    }
+  } else {
+    uint16_t w[PW];
+#pragma unroll
+    for (int i = 0; i < PW; ++i) {
+      const float x = alpha * v[i];
+      uint16_t hb;
+      uint32_t a;
+      if (x != x) {
+        hb = 0x7FFFu;
+        a = 0x7FFFFFFFu;
+      } else if (p.out_dtype == 1) {
+        hb = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+        a = ((uint32_t)hb << 16) & 0x7FFFFFFFu;
+      } else {
+        const __half hv = __float2half_rn(x);
+        hb = __half_as_ushort(hv);
+        a = __float_as_uint(__half2float(hv)) & 0x7FFFFFFFu;
+      }
+      w[i] = hb;
+      if (row_ok && q0 + i < p.Q) amax_local = max(amax_local, a);
+    }
+    if (!p.swap) {
+#pragma unroll
+      for (int c = 0; c < (PW * 2) / 16; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[e] = (uint32_t)w[8 * c + 2 * e] | ((uint32_t)w[8 * c + 2 * e + 1] << 16);
+        const uint32_t off = swz((uint32_t)lane * p.out_rowbytes + c * 16u, p.out_swz_mask);
+        *reinterpret_cast<uint4*>(stg + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < PW; ++i) {
+        const uint32_t off = swz((uint32_t)i * p.out_rowbytes + lane * 2u, p.out_swz_mask);
+        *reinterpret_cast<uint16_t*>(stg + off) = w[i];
+      }
+    }
+  }
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  // A box that starts inside C is clipped by the TMA unit; one that starts
+  // past its end holds nothing to store and is skipped.
+  if (lane == 0 && in_bounds) {
+    ptx::tma_store_3d(tm_c, stg_s, cx, cy, cl);
+    ptx::bulk_commit();
+  }
+}
+
+template <int BN, bool SLOW, bool MX>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8mm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+                 const __grid_constant__ CUtensorMap tm_c, const KParams p) {
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+  static_assert(!MX || BN >= 128, "MX tiles cover whole 128-row scale-factor atoms");
+  static_assert(!SLOW || BN <= 128, "slow accumulation keeps BN/2 fp32 sums per thread in registers");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sraw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (sraw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - sraw);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.stages;
+
+  const uint32_t bar_full = sbase + p.off_bar;
+  const uint32_t bar_empty = bar_full + 8u * S;
+  const uint32_t bar_tfull = bar_empty + 8u * S;
+  const uint32_t bar_tempty = bar_tfull + 16u;
+  const uint32_t bar_epi = bar_tempty + 16u;
+  const uint32_t bar_done = bar_epi + 8u;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sgen + p.off_bar + 16u * S + 48u);
+  // misc[0] TMEM base address, misc[1] abort flag, misc[2] split-K ticket
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(bar_full + 8u * s, 1);
+      ptx::mbar_init(bar_empty + 8u * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar_tfull + 8u * b, 1);
+      ptx::mbar_init(bar_tempty + 8u * b, kEpiWarps);
+    }
+    ptx::mbar_init(bar_epi, kEpiWarps);
+    ptx::mbar_init(bar_done, 1);
+    misc[1] = 0u;
+    misc[2] = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(misc)), p.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem_base = misc[0];
+  volatile uint32_t* abort_flag = misc + 1;
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      long long narm = 0;
+      bool ok = true;
+      const uint32_t tx = p.x_stage_bytes + p.y_stage_bytes + (MX ? 512u * (1 + p.sfy_atoms) : 0u);
+      for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        const Unit t = decode_unit(u, p);
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          if (!wait_bar(bar_empty + 8u * stage, phase ^ 1u, abort_flag, kErrProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8u * stage;
+          ptx::mbar_arrive_expect_tx(fb, tx);
+          ptx::tma_load_3d(sbase + p.off_x + stage * p.x_stage_bytes, &tm_x, fb, kb * kBlockK,
+                           t.tr * kBlockM, t.l);
+          ptx::tma_load_3d(sbase + p.off_y + stage * p.y_stage_bytes, &tm_y, fb, kb * kBlockK,
+                           t.tq * BN, t.l);
+          if constexpr (MX) {
+            const uint32_t sf = sbase + p.off_sf + stage * p.sf_stage_bytes;
+            const uint8_t* gx =
+                p.sfx + (((size_t)t.l * p.sfx_mb + t.tr) * p.scale_kb + kb) * 512u;
+            ptx::bulk_load(sf, gx, 512u, fb);
+            for (int i = 0; i < p.sfy_atoms; ++i) {
+              // atoms past the last row block are clamped to it; their rows are never stored
+              const int mb = min(t.tq * p.sfy_atoms + i, p.sfy_mb - 1);
+              const uint8_t* gy = p.sfy + (((size_t)t.l * p.sfy_mb + mb) * p.scale_kb + kb) * 512u;
+              ptx::bulk_load(sf + 512u * (1 + i), gy, 512u, fb);
+            }
+          }
+          ++narm;
+          if (++stage == (uint32_t)S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Wait until every copy this thread started has landed (all of them
+      // were consumed already unless another role aborted).
+      // (stage, phase) is the next slot: slots below it were last armed in
+      // this pass of the ring, the others in the previous pass.
+      for (int s = 0; s < S; ++s) {
+        if (narm > s) drain_wait(bar_full + 8u * s, ((uint32_t)s < stage) ? phase : (phase ^ 1u));
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
+      bool ok = true;
+      for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        const Unit t = decode_unit(u, p);
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          const bool gstart = SLOW || kb == t.kb0;
+          const bool gend = SLOW || kb == t.kb1 - 1;
+          if (gstart) {
+            if (!wait_bar(bar_tempty + 8u * abuf, aphase ^ 1u, abort_flag, kErrMmaAcc)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after_sync();
+          }
+          if (!wait_bar(bar_full + 8u * stage, phase, abort_flag, kErrMmaFull)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+          const uint32_t d = tmem_base + abuf * BN;
+          const uint64_t adesc = ptx::desc_sw128_kmajor(sbase + p.off_x + stage * p.x_stage_bytes);
+          const uint64_t bdesc = ptx::desc_sw128_kmajor(sbase + p.off_y + stage * p.y_stage_bytes);
+          if constexpr (MX) {
+            const uint32_t sf_smem = sbase + p.off_sf + stage * p.sf_stage_bytes;
+            const uint32_t sf_x = tmem_base + (uint32_t)(p.num_acc * BN) + stage * 16u;
+            const uint32_t sf_y = sf_x + 4u;
+            ptx::tmem_cp_32x128b_warpx4(sf_x, ptx::desc_sf_atom(sf_smem));
+            for (int i = 0; i < p.sfy_atoms; ++i)
+              ptx::tmem_cp_32x128b_warpx4(sf_y + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * (1 + i)));
+#pragma unroll
+            for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+              // scale-factor ids pick byte k of each 32-bit TMEM word: the K block of 32
+              const uint32_t idesc = p.idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4);
+              ptx::mma_mxf8f6f4(d, adesc + 2u * k, bdesc + 2u * k, idesc, sf_x, sf_y,
+                                (!gstart || k > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kBlockK / kUmmaK; ++k)
+              ptx::mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, p.idesc, (!gstart || k > 0) ? 1u : 0u);
+          }
+          ptx::tc_commit(bar_empty + 8u * stage);
+          if (gend) {
+            ptx::tc_commit(bar_tfull + 8u * abuf);
+            if (p.num_acc == 2) {
+              abuf ^= 1u;
+              if (abuf == 0) aphase ^= 1u;
+            } else {
+              aphase ^= 1u;
+            }
+          }
+          if (++stage == (uint32_t)S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: every MMA issued above has completed before TMEM is freed.
+      ptx::tc_commit(bar_done);
+      drain_wait(bar_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    constexpr int HALF = BN / 2;
+    constexpr int PW = HALF < 16 ? HALF : 16;  // columns per output piece
+    constexpr int NPC = HALF / PW;
+    constexpr int LDW = HALF < 32 ? HALF : 32;  // columns per tcgen05.ld while promoting
+    const int qd = warp & 3;                    // TMEM lane quarter this warp may access
+    const int h = warp >> 2;                    // column half
+    const int row = qd * 32 + lane;             // tile row == TMEM lane
+    const int col0 = h * HALF;
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    uint32_t abuf = 0, aphase = 0, epi_phase = 0;
+    uint32_t amax_local = 0;
+    bool ok = true;
+    const float alpha = p.sa_tensor ? (__ldg(p.sa_tensor) * __ldg(p.sb_tensor)) : 1.0f;
+    float* ys_w = reinterpret_cast<float*>(sgen + p.off_ys) + warp * HALF;
+    uint8_t* stg = sgen + p.off_out + warp * kStageOutBytes;
+    const uint32_t stg_s = sbase + p.off_out + warp * kStageOutBytes;
+    float acc[SLOW ? HALF : 1];  // slow accumulation: fp32 running sum of the promoted chunks
+    (void)acc;
+    (void)ys_w;
+
+    for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+      const Unit t = decode_unit(u, p);
+      const int xr = t.tr * kBlockM + row;  // row of X this thread owns
+      const bool row_ok = xr < p.R;
+      if constexpr (SLOW) {
+        // One hand-off per 128-K chunk: acc += s_x(row, c) * s_y(col, c) * chunk.
+        for (int g = 0; g < t.kb1 - t.kb0; ++g) {
+          float xs = 1.0f;
+          if (p.x_kind != kScaleNone) {
+            const int c = t.kb0 + g;
+            if (row_ok) {
+              xs = (p.x_kind == kScaleRow)
+                       ? __ldg(p.x_scale + ((size_t)t.l * p.R + xr) * p.scale_kb + c)
+                       : __ldg(p.x_scale + ((size_t)t.l * ((p.R + 127) / 128) + xr / 128) * p.scale_kb + c);
+            }
+            __syncwarp();
+            for (int j = lane; j < HALF; j += 32) {
+              const int yq = t.tq * BN + col0 + j;
+              float v = 0.0f;
+              if (yq < p.Q) {
+                v = (p.y_kind == kScaleRow)
+                        ? __ldg(p.y_scale + ((size_t)t.l * p.Q + yq) * p.scale_kb + c)
+                        : __ldg(p.y_scale + ((size_t)t.l * ((p.Q + 127) / 128) + yq / 128) * p.scale_kb + c);
+              }
+              ys_w[j] = v;
+            }
+            __syncwarp();
+          }
+          if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, kErrEpiAcc)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+          const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
+#pragma unroll
+          for (int pc = 0; pc < HALF / LDW; ++pc) {
+            uint32_t r[LDW];
+            tmem_load<LDW>(taddr + pc * LDW, r);
+#pragma unroll
+            for (int i = 0; i < LDW; ++i) {
+              const int j = pc * LDW + i;
+              const float v = __uint_as_float(r[i]);
+              if (p.x_kind != kScaleNone) {
+                const float f = xs * ys_w[j];
+                acc[j] = (g == 0) ? f * v : fmaf(f, v, acc[j]);
+              } else {
+                acc[j] = (g == 0) ? v : acc[j] + v;
+              }
+            }
+          }
+          ptx::tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar_tempty + 8u * abuf);
+          if (p.num_acc == 2) {
+            abuf ^= 1u;
+            if (abuf == 0) aphase ^= 1u;
+          } else {
+            aphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      } else {
+        if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, kErrEpiAcc)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after_sync();
+      }
+      // Fast accumulation reads the finished tile from TMEM piece by piece.
+      const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
+      auto get_piece = [&](int pc, float(&v)[PW]) {
+        if constexpr (SLOW) {
+#pragma unroll
+          for (int i = 0; i < PW; ++i) v[i] = acc[pc * PW + i];
+        } else {
+          uint32_t r[PW];
+          tmem_load<PW>(taddr + pc * PW, r);
+#pragma unroll
+          for (int i = 0; i < PW; ++i) v[i] = __uint_as_float(r[i]);
+        }
+      };
+
+      // ---------------------------------------------------- split-K fix-up
+      bool finish = true;
+      float* tile_ws = nullptr;
+      if (p.splits > 1) {
+        const long long tile = ((long long)t.l * p.tiles_r + t.tr) * p.tiles_q + t.tq;
+        tile_ws = p.ws_partials + (size_t)tile * p.splits * (kBlockM * BN);
+        float* slot = tile_ws + (size_t)t.s * (kBlockM * BN);
+#pragma unroll
+        for (int pc = 0; pc < NPC; ++pc) {
+          float v[PW];
+          get_piece(pc, v);
+#pragma unroll
+          for (int i = 0; i < PW; ++i) __stcg(slot + (size_t)(col0 + pc * PW + i) * kBlockM + row, v[i]);
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_epi);
+        if (!wait_bar(bar_epi, epi_phase, abort_flag, kErrEpiSync)) {
+          ok = false;
+          break;
+        }
+        epi_phase ^= 1u;
+        if (warp == 0 && lane == 0) {
+          __threadfence();
+          misc[2] = atomicAdd(p.ws_counters + tile, 1u);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_epi);
+        if (!wait_bar(bar_epi, epi_phase, abort_flag, kErrEpiSync)) {
+          ok = false;
+          break;
+        }
+        epi_phase ^= 1u;
+        finish = misc[2] == (uint32_t)(p.splits - 1);  // the last arrival finishes the tile
+        if (finish) __threadfence();
+      }
+
+      // ---------------------------------------------------- scale, cast, store
+      if (finish) {
+#pragma unroll
+        for (int pc = 0; pc < NPC; ++pc) {
+          float v[PW];
+          get_piece(pc, v);
+          if (p.splits > 1) {
+            // Partials are added in split order 0..S-1 whichever CTA arrived last.
+#pragma unroll
+            for (int i = 0; i < PW; ++i) {
+              const size_t off = (size_t)(col0 + pc * PW + i) * kBlockM + row;
+              float sum = (t.s == 0) ? v[i] : __ldcg(tile_ws + off);
+              for (int ss = 1; ss < p.splits; ++ss)
+                sum += (ss == t.s) ? v[i] : __ldcg(tile_ws + (size_t)ss * (kBlockM * BN) + off);
+              v[i] = sum;
+            }
+          }
+          const int q0 = t.tq * BN + col0 + pc * PW;  // Y row of the piece's first column
+          const int r0 = t.tr * kBlockM + qd * 32;    // X row of the warp's first lane
+          store_piece<PW>(p, &tm_c, v, alpha, row_ok, q0, lane, stg, stg_s, p.swap ? r0 : q0,
+                          p.swap ? q0 : r0, t.l, q0 < p.Q && r0 < p.R, amax_local);
+        }
+      }
+      if constexpr (!SLOW) {
+        ptx::tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_tempty + 8u * abuf);
+        if (p.num_acc == 2) {
+          abuf ^= 1u;
+          if (abuf == 0) aphase ^= 1u;
+        } else {
+          aphase ^= 1u;
+        }
+      }
+    }
+    if (lane == 0) ptx::bulk_wait_all();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax_local = max(amax_local, __shfl_xor_sync(0xFFFFFFFFu, amax_local, o));
+    if (lane == 0 && amax_local != 0u) atomicMax(p.amax_bits, amax_local);
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+}  // namespace fp8mm

@@ -1,0 +1,119 @@
+"""CPU checks of the C ABI: the library builds and loads, exports every symbol
+include/fp8mm.h declares, and rejects invalid descriptions before touching
+CUDA (so these run on a machine without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from precision_matmul_gb300 import _binding as B
+from precision_matmul_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return B.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "fp8mm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8mm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared_functions() == sorted(B.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_structs_match_the_header_layout(tmp_path):
+    # compile the header with gcc and compare every field offset with ctypes
+    import subprocess
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "fp8mm.h"', 'int main(void) {']
+    for cname, cls in (("fp8mm_desc", B.fp8mm_desc), ("fp8mm_plan_info", B.fp8mm_plan_info)):
+        lines.append(f'printf("%zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("%zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I" + os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = []
+    for cls in (B.fp8mm_desc, B.fp8mm_plan_info):
+        want.append(ctypes.sizeof(cls))
+        want += [getattr(cls, f).offset for f, _ in cls._fields_]
+    assert got == want
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert B.fp8mm_status_string(code)
+    assert B.fp8mm_status_string(99) == "unknown status"
+
+
+def _plan_status(**kw):
+    d = B.make_desc(**kw)
+    h = ctypes.c_void_p()
+    st = B.load().fp8mm_plan(ctypes.byref(d), ctypes.byref(h))
+    if h.value:
+        B.load().fp8mm_destroy(h)
+    return st
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1, N=16, K=16), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, a_fmt=2), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, out_dtype=3), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, scale_mode=4), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, fast_accum=2), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, block_n=48), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, swap_ab=3), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=24), B.FP8MM_ERR_ALIGNMENT),          # K rows not 16-byte multiples
+    (dict(M=16, N=12, K=16), B.FP8MM_ERR_ALIGNMENT),          # bf16 C rows of 24 bytes
+    (dict(M=16, N=4, K=16, out_dtype=0), B.FP8MM_OK),         # fp32 rows of 16 bytes pass validation
+    (dict(M=16, N=16, K=16, scale_mode=3, a_fmt=0, b_fmt=1), B.FP8MM_ERR_UNSUPPORTED),
+    (dict(M=2 ** 31, N=16, K=16), B.FP8MM_ERR_UNSUPPORTED),
+])
+def test_plan_validation_before_cuda(lib, kw, status):
+    st = _plan_status(**kw)
+    if status == B.FP8MM_OK:
+        # valid descriptions reach the device query, which fails without a GPU
+        assert st in (B.FP8MM_OK, B.FP8MM_ERR_CUDA)
+    else:
+        assert st == status
+
+
+def test_reserved_fields_must_be_zero(lib):
+    d = B.make_desc(16, 16, 16)
+    d.reserved[1] = 7
+    h = ctypes.c_void_p()
+    assert B.load().fp8mm_plan(ctypes.byref(d), ctypes.byref(h)) == B.FP8MM_ERR_INVALID
+
+
+def test_null_arguments(lib):
+    h = ctypes.c_void_p()
+    assert B.load().fp8mm_plan(None, ctypes.byref(h)) == B.FP8MM_ERR_INVALID
+    assert B.load().fp8mm_run(None, None, None, None, None, None, None, None, 0, None) == B.FP8MM_ERR_INVALID
+    n = ctypes.c_size_t()
+    assert B.load().fp8mm_workspace_size(None, ctypes.byref(n)) == B.FP8MM_ERR_INVALID
+
+
+def test_product_path_has_no_oracle_dependency():
+    # the package must never import the oracle (it is test infrastructure)
+    pkg = os.path.join(ROOT, "precision_matmul_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "fp8_oracle" not in text, f

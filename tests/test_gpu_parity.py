@@ -1,0 +1,166 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Sizes here finish in seconds on the oracle yet span several tiles with ragged
+edges in M, N and K; the full workload sizes are in test_gpu_full.py.
+Bound: |C_gpu - C_exact| <= K 2^-23 sum|a_hat b_hat| + half an ulp of out_dtype
+(see tests/parity.py); amax bit-equal to max |C| of the GPU's own C.
+"""
+import numpy as np
+import pytest
+import torch
+
+import precision_matmul_gb300 as pm
+from precision_matmul_gb300 import synth
+
+from parity import amax_bits_of, check, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_check(p, **kw):
+    c, amax, plan = run_gpu(p, **kw)
+    torch.cuda.synchronize()
+    assert pm.fp8mm_device_error(0) == 0
+    check(p, c, amax)
+    return c, amax, plan
+
+
+def test_tiny_per_tensor_fp32():
+    # 256^3, E4M3, scales 0.5 / 2.0, fast accumulation, fp32 out
+    _run_check(synth.tiny_per_tensor())
+
+
+@pytest.mark.parametrize("out", [synth.OUT_BF16, synth.OUT_F16, synth.OUT_F32])
+@pytest.mark.parametrize("fast", [True, False])
+def test_per_tensor_ragged(out, fast):
+    p = synth.llm_per_tensor(M=300, N=264, K=528, seed=11, fast_accum=fast, out_dtype=out)
+    if out == synth.OUT_F16:
+        # keep the fp16 range: scales 2^-4 .. 1
+        p.scale_a.fill_(0.0625)
+        p.scale_b.fill_(0.5)
+    _run_check(p)
+
+
+@pytest.mark.parametrize("block_n", [16, 32, 64, 128, 256])
+def test_per_tensor_every_tile_width(block_n):
+    p = synth.llm_per_tensor(M=260, N=520, K=384, seed=12, fast_accum=True)
+    _run_check(p, block_n=block_n, swap_ab=2)
+
+
+@pytest.mark.parametrize("fmts", [(0, 1), (1, 0), (1, 1)])
+def test_e5m2_operand_pairs(fmts):
+    g = torch.Generator().manual_seed(13)
+    M, N, K = 200, 136, 256
+    a = synth.cast_fp8(torch.randn(1, M, K, generator=g) * 300, fmts[0])
+    b = synth.cast_fp8(torch.randn(1, N, K, generator=g) * 300, fmts[1])
+    one = torch.tensor([0.25], dtype=torch.float32)
+    p = synth.Problem("pairs", 1, M, N, K, a, b, one, one.clone(), fmts[0], fmts[1], synth.SCALE_TENSOR,
+                      synth.OUT_F32, True)
+    _run_check(p)
+
+
+@pytest.mark.parametrize("mode", [synth.SCALE_A1x128_B128x128, synth.SCALE_A1x128_B1x128])
+def test_blockwise_ragged(mode):
+    p = synth.blockwise(M=272, N=392, K=640, seed=14, b_block=128 if mode == synth.SCALE_A1x128_B128x128 else 1)
+    _run_check(p)
+
+
+@pytest.mark.parametrize("fmt", [synth.E4M3, synth.E5M2])
+def test_mx_batched(fmt):
+    p = synth.mx_batched(L=2, M=256, N=384, K=512, fmt=fmt, seed=15)
+    _run_check(p)
+
+
+def test_mx_ragged():
+    p = synth.mx_batched(L=3, M=200, N=136, K=320, seed=16)
+    _run_check(p)
+
+
+@pytest.mark.parametrize("M", [16, 40, 64, 200])
+@pytest.mark.parametrize("data", ["gauss40", "adversarial"])
+@pytest.mark.parametrize("fast", [True, False])
+def test_skinny_swap_ab_split_k(M, data, fast):
+    p = synth.skinny(M=M, N=1536, K=2048, data=data, seed=17, fast_accum=fast)
+    c, amax, plan = _run_check(p)
+    info = plan.info()
+    assert info["swap_ab"] == 1
+
+
+@pytest.mark.parametrize("splitk", [2, 3, 5])
+def test_forced_split_k_non_swapped(splitk):
+    p = synth.llm_per_tensor(M=384, N=512, K=1280, seed=18, fast_accum=True)
+    c, amax, plan = _run_check(p, splitk=splitk, swap_ab=2)
+    assert plan.info()["splitk"] == splitk
+
+
+def test_blockwise_split_k_swapped():
+    p = synth.blockwise(M=48, N=512, K=1536, seed=19)
+    c, amax, plan = _run_check(p, splitk=3, swap_ab=1)
+    assert plan.info()["swap_ab"] == 1 and plan.info()["splitk"] == 3
+
+
+def test_smoke_gate_cases():
+    _run_check(synth.random_codes(16, 8, 64))
+    _run_check(synth.adversarial_codes(64, 64, 256))
+
+
+def test_special_values_nan_inf():
+    # E5M2 Inf and NaN codes: Inf * 0 -> NaN, Inf + finite -> Inf; NaN output canonical, amax NaN
+    g = torch.Generator().manual_seed(20)
+    M, N, K = 130, 40, 64
+    a = synth.cast_fp8(torch.randn(1, M, K, generator=g), synth.E5M2)
+    b = synth.cast_fp8(torch.randn(1, N, K, generator=g), synth.E5M2)
+    a[0, 3, 5] = 0x7C      # +Inf
+    a[0, 7, :] = 0         # zeros ...
+    a[0, 7, 9] = 0x7C      # ... and +Inf: NaN where B[n, 9] == 0, else +-Inf
+    b[0, 2, 9] = 0
+    a[0, 11, 1] = 0x7F     # NaN code
+    one = torch.tensor([1.0], dtype=torch.float32)
+    for out in (synth.OUT_F32, synth.OUT_BF16):
+        p = synth.Problem("special", 1, M, N, K, a, b, one, one.clone(), synth.E5M2, synth.E5M2,
+                          synth.SCALE_TENSOR, out, True)
+        c, amax, _ = _run_check(p)
+        assert int(amax.view(torch.int32).item()) == 0x7FFFFFFF
+
+
+def test_empty_and_zero_k():
+    dev = torch.device("cuda:0")
+    for (M, N, K) in [(0, 64, 64), (64, 0, 64), (64, 64, 0)]:
+        a = torch.zeros(M, K, dtype=torch.uint8, device=dev)
+        b = torch.zeros(N, K, dtype=torch.uint8, device=dev)
+        s = torch.ones(1, dtype=torch.float32, device=dev)
+        c, amax = pm.scaled_mm(a, b, s, s, out_dtype=torch.bfloat16, a_fmt=0, b_fmt=0)
+        torch.cuda.synchronize()
+        assert c.shape == (M, N)
+        if c.numel():
+            assert (c.float() == 0).all()
+        assert float(amax) == 0.0
+
+
+def test_deterministic_repeat():
+    p = synth.skinny(M=64, N=1024, K=4096, seed=21)
+    t = to_device(p)
+    c1, a1, _ = run_gpu(p, tensors=t)
+    c1 = c1.clone()
+    a1 = a1.clone()
+    c2, a2, _ = run_gpu(p, tensors=t)
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+    assert torch.equal(a1.view(torch.int32), a2.view(torch.int32))
+
+
+def test_out_prior_contents_do_not_matter():
+    p = synth.llm_per_tensor(M=128, N=256, K=256, seed=22, fast_accum=True)
+    a, b, sa, sb = to_device(p)
+    out = torch.full((128, 256), float("nan"), dtype=torch.bfloat16, device="cuda:0")
+    amax = torch.full((1,), 12345.0, dtype=torch.float32, device="cuda:0")
+    c, am = pm.scaled_mm(a[0], b[0], sa, sb, out=out, amax=amax, use_fast_accum=True, a_fmt=0, b_fmt=0)
+    torch.cuda.synchronize()
+    assert not torch.isnan(c.float()).any()
+    assert int(am.view(torch.int32).item()) == amax_bits_of(c)
+
+
+def test_launch_count_is_one_kernel():
+    p = synth.llm_per_tensor(M=256, N=256, K=256, seed=23)
+    _, _, plan = run_gpu(p)
+    assert plan.kernel_launches() == 1
