@@ -95,6 +95,8 @@ cudaError_t ensure_smem_attr(KernelFn fn, int device, size_t bytes) {
       if (done[device][i] == (const void*)fn) return cudaSuccess;
     }
   }
+  // Opt in to the device's full limit once, so that any later plan of the
+  // same kernel (another stage count or layout) fits as well.
   cudaError_t e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   if (device >= 0 && device < 64) {
@@ -528,7 +530,7 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
 
   KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
-  if (ensure_smem_attr(fn, d.device, P->smem_bytes) != cudaSuccess) return FP8MM_ERR_CUDA;
+  if (ensure_smem_attr(fn, d.device, (size_t)P->max_smem) != cudaSuccess) return FP8MM_ERR_CUDA;
   void* args[4] = {&tm_x, &tm_y, &tm_c, &kp};
   cudaError_t e = cudaLaunchKernel((const void*)fn, dim3((unsigned)P->grid), dim3(kThreads), args, P->smem_bytes,
                                    stream);
