@@ -149,6 +149,33 @@ fp8mm_status fp8mm_device_error(int device, uint32_t* code, int clear);
  * and, with split-K, the counter reset are stream memsets, not kernels). */
 fp8mm_status fp8mm_plan_kernel_launches(const fp8mm_plan_t* plan, int32_t* launches);
 
+/* Largest split-K scratch fp8mm_run_static_workspace can serve (16 MiB). */
+#define FP8MM_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+
+/* fp8mm_run for callers that cannot allocate device memory -- for example a
+ * plugin or custom-call host that owns every device buffer and hands an
+ * operation only its inputs and outputs, or a service whose device-memory
+ * budget is fixed once it has started.  The pages have no counterpart of this
+ * entry point; it exists for such callers.
+ *
+ * Same arguments and results as fp8mm_run minus the workspace: split-K
+ * scratch comes from one array of FP8MM_STATIC_WORKSPACE_BYTES bytes that the
+ * library defines in device memory and that every GPU which loads the library
+ * keeps until the process exits.  Nothing is allocated or freed by this call.
+ *   - A plan whose fp8mm_workspace_size exceeds FP8MM_STATIC_WORKSPACE_BYTES
+ *     is rejected with FP8MM_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device that needs scratch looks up the array's
+ *     device address (cudaGetSymbolAddress, with that device current); make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents.  Each call resets the parts that must start at zero on its
+ *     stream, so calls in stream order are independent; calls that may run
+ *     at the same time on the GPU (other streams, other threads) race on the
+ *     array and give undefined results. */
+fp8mm_status fp8mm_run_static_workspace(fp8mm_plan_t* plan, const void* a, const void* b,
+                                        const void* scale_a, const void* scale_b, void* c,
+                                        float* amax, void* stream);
+
 /* One-shot form: plan, run, destroy.  Same arguments as fp8mm_plan + fp8mm_run. */
 fp8mm_status fp8mm_gemm(const fp8mm_desc* desc, const void* a, const void* b,
                         const void* scale_a, const void* scale_b, void* c, float* amax,

@@ -24,7 +24,8 @@ FP8MM_ERR_REJECTED, FP8MM_ERR_WORKSPACE, FP8MM_ERR_CUDA, FP8MM_ERR_DEVICE = 4, 5
 # Every symbol include/fp8mm.h declares.
 EXPORTS = ("fp8mm_plan", "fp8mm_workspace_size", "fp8mm_run", "fp8mm_plan_roofline",
            "fp8mm_plan_get_info", "fp8mm_destroy", "fp8mm_status_string", "fp8mm_device_error",
-           "fp8mm_plan_kernel_launches", "fp8mm_gemm")
+           "fp8mm_plan_kernel_launches", "fp8mm_gemm", "fp8mm_run_static_workspace")
+FP8MM_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 
 class fp8mm_desc(ctypes.Structure):
@@ -80,6 +81,8 @@ def load():
     lib.fp8mm_plan_kernel_launches.restype = i32
     lib.fp8mm_gemm.argtypes = [ctypes.POINTER(fp8mm_desc), vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.fp8mm_gemm.restype = i32
+    lib.fp8mm_run_static_workspace.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.fp8mm_run_static_workspace.restype = i32
     _lib = lib
     return lib
 
@@ -167,3 +170,11 @@ def fp8mm_gemm(desc: fp8mm_desc, a_ptr, b_ptr, sa_ptr, sb_ptr, c_ptr, amax_ptr, 
     st = load().fp8mm_gemm(ctypes.byref(desc), a_ptr, b_ptr, sa_ptr, sb_ptr, c_ptr, amax_ptr, ws_ptr,
                            ctypes.c_size_t(int(ws_bytes)), stream)
     _check(st, "fp8mm_gemm")
+
+
+def fp8mm_run_static_workspace(plan: Plan, a_ptr, b_ptr, sa_ptr, sb_ptr, c_ptr, amax_ptr, stream=None) -> None:
+    """fp8mm_run without a caller workspace: split-K scratch comes from the
+    library's fixed device array (FP8MM_STATIC_WORKSPACE_BYTES), so this call
+    allocates nothing; see include/fp8mm.h for the sharing rules."""
+    st = load().fp8mm_run_static_workspace(plan.handle, a_ptr, b_ptr, sa_ptr, sb_ptr, c_ptr, amax_ptr, stream)
+    _check(st, "fp8mm_run_static_workspace")

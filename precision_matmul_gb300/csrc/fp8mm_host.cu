@@ -538,6 +538,56 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   return FP8MM_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Entry point for callers that may not allocate device memory.
+//
+// Split-K plans need scratch memory for their partial tiles and arrival
+// counters.  fp8mm_run takes it from the caller; fp8mm_run_static_workspace
+// instead uses this file-scope array, which every GPU that loads the library
+// holds until the process exits.  Host code only sees a stand-in for the
+// array's name, so its device address is looked up per device with
+// cudaGetSymbolAddress, once, with that device current.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_fp8mm_static_workspace[FP8MM_STATIC_WORKSPACE_BYTES];
+
+static fp8mm_status static_workspace_address(int device, void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  if (device < 0 || device >= 64) return FP8MM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[device]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_fp8mm_static_workspace);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return FP8MM_ERR_CUDA;
+    }
+    addr[device] = p;
+  }
+  *out = addr[device];
+  return FP8MM_OK;
+}
+
+fp8mm_status fp8mm_run_static_workspace(fp8mm_plan_t* plan, const void* a, const void* b, const void* scale_a,
+                                        const void* scale_b, void* c, float* amax, void* stream) {
+  if (!plan) return FP8MM_ERR_INVALID;
+  if (plan->ws_bytes > (size_t)FP8MM_STATIC_WORKSPACE_BYTES) return FP8MM_ERR_WORKSPACE;
+  void* ws = nullptr;
+  if (plan->ws_bytes > 0) {
+    const int dev = plan->d.device;
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) return FP8MM_ERR_CUDA;
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) return FP8MM_ERR_CUDA;
+    const fp8mm_status st = static_workspace_address(dev, &ws);
+    if (prev != dev) cudaSetDevice(prev);
+    if (st != FP8MM_OK) return st;
+  }
+  // fp8mm_run zeroes the arrival counters on the stream before the kernel, and
+  // every partial tile is written before it is read, so leftovers of an earlier
+  // call never leak into this one.
+  return fp8mm_run(plan, a, b, scale_a, scale_b, c, amax, ws, plan->ws_bytes, stream);
+}
+
 fp8mm_status fp8mm_gemm(const fp8mm_desc* desc, const void* a, const void* b, const void* scale_a,
                         const void* scale_b, void* c, float* amax, void* workspace, size_t workspace_bytes,
                         void* stream) {
