@@ -346,7 +346,7 @@ def run_ours(args, rank, world, local_rank):
     hbm, bf16, bf16_sus, peak_src = read_peaks()
     fp8_peak = bf16 * FP8_PER_BF16
     plans = [pm.plan_for((p.M, p.N, p.K, p.L, p.a_fmt, p.b_fmt, p.scale_mode, p.out_dtype,
-                          1 if p.fast_accum else 0, 0, 0, 0, local_rank)) for p in probs]
+                          1 if p.fast_accum else 0, 0, 0, 0, local_rank, 0)) for p in probs]
     rf = [pl.roofline() for pl in plans]
     launches = sum(pl.kernel_launches() for pl in plans)
     avg_launch_s = step_s / max(1, launches)

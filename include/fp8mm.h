@@ -92,10 +92,11 @@ typedef struct {
                           register accumulator.  The block-scale modes always promote per
                           128-K chunk (their scales change per chunk). */
   int32_t splitk;      /* 0: choose; S >= 1: split K into S contiguous 128-aligned ranges */
-  int32_t swap_ab;     /* -1 or 0 in a zeroed struct means choose; 1 force on; 2 force off */
+  int32_t swap_ab;     /* 0: choose; 1: force on; 2: force off */
   int32_t block_n;     /* 0: choose; else the tile width on the MMA's N side (16..256) */
   int32_t device;      /* CUDA device ordinal the plan is for */
-  int32_t reserved[3]; /* must be 0 */
+  int32_t cta_pair;    /* two-SM (CTA pair) tiles: 0 choose; 1 force on; 2 force off */
+  int32_t reserved[2]; /* must be 0 */
 } fp8mm_desc;
 
 typedef struct fp8mm_plan_s fp8mm_plan_t;
@@ -103,7 +104,7 @@ typedef struct fp8mm_plan_s fp8mm_plan_t;
 /* What a plan chose (for reports and tests). */
 typedef struct {
   int32_t swap_ab;      /* 1 if B plays the MMA's A operand (skinny M) */
-  int32_t block_m;      /* rows per tile on the MMA's M side (128) */
+  int32_t block_m;      /* rows per CTA on the MMA's M side (128) */
   int32_t block_n;      /* tile width on the MMA's N side */
   int32_t splitk;       /* K ranges per output tile */
   int32_t stages;       /* shared-memory pipeline depth */
@@ -111,6 +112,7 @@ typedef struct {
   int64_t units;        /* (tile, K range) work units */
   int32_t slow;         /* 1 if 128-K chunks are promoted in registers */
   int32_t smem_bytes;   /* dynamic shared memory per CTA */
+  int32_t cta_pair;     /* 1 if tiles are computed by CTA pairs with two-SM MMAs (256-row tiles) */
 } fp8mm_plan_info;
 
 /* Validate desc and choose tiles, swap-AB and split-K for the device.  On

@@ -20,7 +20,7 @@ struct fp8mm_plan_s {
   int sms = 0;
   int max_smem = 0;
   int swap = 0, bn = 0, splits = 1, kb_per_split = 0, num_kb = 0, stages = 0, num_acc = 2;
-  int group = 1, slow = 0, mx = 0, out_es = 4;
+  int group = 1, slow = 0, mx = 0, out_es = 4, cg = 1;
   int64_t R = 0, Q = 0;
   int tiles_r = 0, tiles_q = 0;
   long long units = 0;
@@ -37,12 +37,21 @@ namespace {
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const KParams);
 
-template <int BN, bool SLOW, bool MX>
+template <int BN, bool SLOW, bool MX, int CG = 1>
 KernelFn kfn() {
-  return &fp8mm_kernel<BN, SLOW, MX>;
+  return &fp8mm_kernel<BN, SLOW, MX, CG>;
 }
 
-KernelFn select_kernel(int bn, bool slow, bool mx) {
+// Instantiated kernels.  Pair (two-SM) tiles: 256 x 256 for fast accumulation
+// and 256 x 128 for slow accumulation (whose promotion keeps BN/2 sums per
+// thread in registers); single-CTA tiles for everything else.
+KernelFn select_kernel(int bn, bool slow, bool mx, int cg) {
+  if (cg == 2) {
+    if (mx) return nullptr;
+    if (bn == 256 && !slow) return kfn<256, false, false, 2>();
+    if (bn == 128) return slow ? kfn<128, true, false, 2>() : kfn<128, false, false, 2>();
+    return nullptr;
+  }
   if (mx) {
     switch (bn) {
       case 128: return slow ? kfn<128, true, true>() : kfn<128, false, true>();
@@ -113,7 +122,7 @@ cudaError_t ensure_smem_attr(KernelFn fn, int device, size_t bytes) {
 // Shared-memory layout for a given stage count; returns total bytes.
 size_t layout(fp8mm_plan_s* P, int stages) {
   const uint32_t x_bytes = kBlockM * kBlockK;
-  const uint32_t y_bytes = (uint32_t)P->bn * kBlockK;
+  const uint32_t y_bytes = (uint32_t)(P->bn / P->cg) * kBlockK;
   const uint32_t sf_bytes = P->mx ? 512u * (1u + (uint32_t)(P->bn / 128)) : 0u;
   uint32_t off = 0;
   P->x_stage_bytes = x_bytes;
@@ -166,7 +175,8 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   if (d.scale_mode < 0 || d.scale_mode > 3) return FP8MM_ERR_INVALID;
   if (d.fast_accum < 0 || d.fast_accum > 1) return FP8MM_ERR_INVALID;
   if (d.splitk < 0 || d.swap_ab < 0 || d.swap_ab > 2 || d.device < 0) return FP8MM_ERR_INVALID;
-  if (d.reserved[0] || d.reserved[1] || d.reserved[2]) return FP8MM_ERR_INVALID;
+  if (d.cta_pair < 0 || d.cta_pair > 2) return FP8MM_ERR_INVALID;
+  if (d.reserved[0] || d.reserved[1]) return FP8MM_ERR_INVALID;
   if (d.block_n != 0 && d.block_n != 16 && d.block_n != 32 && d.block_n != 64 && d.block_n != 128 &&
       d.block_n != 256)
     return FP8MM_ERR_INVALID;
@@ -234,24 +244,43 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     return FP8MM_ERR_UNSUPPORTED;
   }
   P->bn = bn;
+  // Two-SM pair tiles (cta_group::2): each SM stages its 128 rows of X and
+  // half of the Y tile, so a K step moves a third fewer bytes per MMA cycle
+  // into shared memory than a single-CTA 128 x 256 tile.
+  {
+    const bool pair_ok = !mx && (P->slow ? bn == 128 : (bn == 256 || bn == 128));
+    if (d.cta_pair == 1) {
+      if (!pair_ok) {
+        delete P;
+        return FP8MM_ERR_UNSUPPORTED;
+      }
+      P->cg = 2;
+    } else if (d.cta_pair == 0) {
+      // Slow accumulation stays on single-CTA tiles: its per-chunk hand-off
+      // would wait on both CTAs' epilogues.
+      P->cg = (pair_ok && !swap && !P->slow && P->R >= 256 && bn == 256) ? 2 : 1;
+    }
+  }
+  const int64_t tiles_r_cg = std::max<int64_t>(1, cdiv(P->R, (int64_t)kBlockM * P->cg));
   const int64_t tiles_q = std::max<int64_t>(1, cdiv(P->Q, bn));
-  P->tiles_r = (int)tiles_r;
+  P->tiles_r = (int)tiles_r_cg;
   P->tiles_q = (int)tiles_q;
-  const int64_t tiles = tiles_r * tiles_q * std::max<int64_t>(1, d.L);
+  const int64_t tiles = tiles_r_cg * tiles_q * std::max<int64_t>(1, d.L);  // pair tiles when cg == 2
 
   // Split-K: contiguous 128-aligned K ranges.  Chosen to fill whole waves of
   // SMs when there are fewer than two waves of tiles and the partial tiles
   // are small next to the operand bytes they save.
   int S = d.splitk;
+  const int64_t slots = P->sms / P->cg;  // concurrent work units (CTAs or CTA pairs)
   if (S == 0) {
     S = 1;
-    if (tiles < 2 * (int64_t)P->sms && P->num_kb >= 8) {
-      double best = (double)tiles / (double)(cdiv(tiles, P->sms) * P->sms);
+    if (tiles < 2 * (int64_t)slots && P->num_kb >= 8) {
+      double best = (double)tiles / (double)(cdiv(tiles, slots) * slots);
       for (int s = 2; s <= 8; ++s) {
         if (P->num_kb / s < 4) break;
         if (bn > 128 && s > 2) break;
         const int64_t u = tiles * s;
-        const double eff = (double)u / (double)(cdiv(u, P->sms) * P->sms);
+        const double eff = (double)u / (double)(cdiv(u, slots) * slots);
         if (eff > best + 0.05) {
           best = eff;
           S = s;
@@ -263,7 +292,7 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   P->kb_per_split = P->num_kb > 0 ? (int)cdiv(P->num_kb, S) : 0;
   P->splits = P->num_kb > 0 ? (int)cdiv(P->num_kb, P->kb_per_split) : 1;
   P->units = (long long)tiles * P->splits;
-  P->grid = (int)std::min<long long>(P->units, P->sms);
+  P->grid = (int)std::min<long long>(P->units * P->cg, P->sms / P->cg * P->cg);
   P->group = swap ? 1 : 8;
 
   // TMEM: accumulators, then (MX) a ring of scale-factor slots of 16 columns.
@@ -287,10 +316,33 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   }
   P->tmem_cols = cols;
 
+  if (P->cg == 2) {
+    // Persistent grid: as many CTA pairs as can be resident at once.
+    KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg);
+    int nclusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)P->grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = P->smem_bytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!fn || ensure_smem_attr(fn, d.device, (size_t)P->max_smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&nclusters, (const void*)fn, &cfg) != cudaSuccess || nclusters < 1) {
+      cudaGetLastError();
+      delete P;
+      return FP8MM_ERR_CUDA;
+    }
+    P->grid = 2 * (int)std::min<long long>(P->units, nclusters);
+  }
   if (P->splits > 1) {
-    P->ws_partials_bytes = (size_t)tiles * P->splits * kBlockM * bn * sizeof(float);
+    P->ws_partials_bytes = (size_t)tiles * P->cg * P->splits * kBlockM * bn * sizeof(float);
     P->ws_counters_off = (P->ws_partials_bytes + 255) & ~(size_t)255;
-    P->ws_counters_bytes = (size_t)tiles * sizeof(unsigned);
+    P->ws_counters_bytes = (size_t)tiles * P->cg * sizeof(unsigned);
     P->ws_bytes = P->ws_counters_off + ((P->ws_counters_bytes + 255) & ~(size_t)255);
   }
   *out = P;
@@ -333,6 +385,7 @@ fp8mm_status fp8mm_plan_get_info(const fp8mm_plan_t* plan, fp8mm_plan_info* info
   info->units = plan->units;
   info->slow = plan->slow;
   info->smem_bytes = (int32_t)plan->smem_bytes;
+  info->cta_pair = plan->cg == 2 ? 1 : 0;
   return FP8MM_OK;
 }
 
@@ -422,25 +475,26 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   {
     cuuint64_t dims[3] = {(cuuint64_t)d.K, (cuuint64_t)P->Q, (cuuint64_t)d.L};
     cuuint64_t strides[2] = {(cuuint64_t)d.K, (cuuint64_t)(d.K * P->Q)};
-    cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)P->bn, 1};
+    cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)(P->bn / P->cg), 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(&tm_y, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(yptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return FP8MM_ERR_CUDA;
   }
-  const int half = P->bn / 2;
-  const int pw = half < 16 ? half : 16;
+  // One TMA store per warp covers 32 tile rows x `cw` tile columns, staged in
+  // shared memory with the swizzle that matches its row length.
+  const int cw = chunk_cols(P->bn, P->out_es);
   uint32_t rowbytes;
   cuuint32_t cbox[3];
   if (!P->swap) {
-    rowbytes = (uint32_t)(pw * P->out_es);
-    cbox[0] = (cuuint32_t)pw;
+    rowbytes = (uint32_t)(cw * P->out_es);
+    cbox[0] = (cuuint32_t)cw;
     cbox[1] = 32;
   } else {
     rowbytes = (uint32_t)(32 * P->out_es);
     cbox[0] = 32;
-    cbox[1] = (cuuint32_t)pw;
+    cbox[1] = (cuuint32_t)cw;
   }
   cbox[2] = 1;
   CUtensorMapSwizzle cswz;
@@ -488,11 +542,11 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
     // kind::mxf8f6f4: B scale id bits 4-5, formats 7-9 / 10-12, N>>3 at 17, UE8M0 scale type bit 23,
     // M>>4 at 24, A scale id bits 29-30 (ids added per K step in the kernel).
     kp.idesc = (xf << 7) | (yf << 10) | ((uint32_t)(P->bn >> 3) << 17) | (1u << 23) |
-               ((uint32_t)(kBlockM >> 4) << 24);
+               ((uint32_t)((kBlockM * P->cg) >> 4) << 24);
   } else {
     // kind::f8f6f4: fp32 accumulator (bits 4-5 = 1), formats, K-major A and B, N>>3 at 17, M>>4 at 24.
     kp.idesc = (1u << 4) | (xf << 7) | (yf << 10) | ((uint32_t)(P->bn >> 3) << 17) |
-               ((uint32_t)(kBlockM >> 4) << 24);
+               ((uint32_t)((kBlockM * P->cg) >> 4) << 24);
   }
   if (d.scale_mode == FP8MM_SCALE_TENSOR) {
     kp.sa_tensor = static_cast<const float*>(scale_a);
@@ -528,13 +582,23 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   kp.out_swz_mask = swz_mask;
   kp.out_rowbytes = rowbytes;
 
-  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0);
+  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
   if (ensure_smem_attr(fn, d.device, (size_t)P->max_smem) != cudaSuccess) return FP8MM_ERR_CUDA;
   void* args[4] = {&tm_x, &tm_y, &tm_c, &kp};
-  cudaError_t e = cudaLaunchKernel((const void*)fn, dim3((unsigned)P->grid), dim3(kThreads), args, P->smem_bytes,
-                                   stream);
-  if (e != cudaSuccess) return FP8MM_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P->cg;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)P->grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = P->smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = P->cg == 2 ? 1 : 0;
+  if (cudaLaunchKernelExC(&cfg, (const void*)fn, args) != cudaSuccess) return FP8MM_ERR_CUDA;
   return FP8MM_OK;
 }
 

@@ -47,7 +47,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kProdWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
-constexpr int kStageOutBytes = 2048;  // per-warp output staging buffer
+constexpr int kStageOutBytes = 4096;  // per-warp output staging: two 2 KiB buffers
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 
 // Abort codes (OR-ed into the device word).
@@ -167,99 +167,362 @@ __device__ __forceinline__ uint32_t swz(uint32_t off, uint32_t mask) {
   return off ^ (((off >> 7) & mask) << 4);
 }
 
-// Scales PW values of this thread's tile row, casts them to out_dtype
-// (round to nearest even; NaN becomes the canonical pattern), folds |value|
-// into the running amax (rows and columns inside C only), stages the warp's
-// 32 x PW block in shared memory and stores it with one TMA copy at (cx, cy, cl).
-template <int PW>
-__device__ __forceinline__ void store_piece(const KParams& p, const CUtensorMap* tm_c, const float (&v)[PW],
-                                            float alpha, bool row_ok, int q0, int lane, uint8_t* stg,
-                                            uint32_t stg_s, int cx, int cy, int cl, bool in_bounds,
-                                            uint32_t& amax_local) {
-  if (lane == 0) ptx::bulk_wait_read_all();  // the previous store has read the staging buffer
-  __syncwarp();
-  if (p.out_es == 4) {
-    uint32_t w[PW];
+// Columns of one output chunk: staging rows of 64 bytes (32 bf16/fp16 or 16
+// fp32 values), or the whole column range of a warp when that is narrower.
+__host__ __device__ constexpr int chunk_cols(int bn, int es) {
+  return (es == 4) ? (bn >= 32 ? 16 : bn / 2) : (bn >= 64 ? 32 : bn / 2);
+}
+// Columns [0, half0_cols) belong to epilogue warps 0-3, the rest to warps 4-7.
+__host__ __device__ constexpr int half0_cols(int bn) { return bn <= 64 ? bn / 2 : ((bn / 2 + 31) / 32) * 32; }
+
+// Packed fp32 pairs (Blackwell f32x2 arithmetic).
+__device__ __forceinline__ void mul2(float& x0, float& x1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(x0), "=f"(x1)
+      : "f"(x0), "f"(x1), "f"(a0), "f"(a1));
+}
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(c0), "=f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& c0, float& c1, float b0, float b1) {
+  asm("{\n\t.reg .b64 rb, rc, rd;\n\tmov.b64 rb, {%2, %3};\n\tmov.b64 rc, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, rc, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(c0), "=f"(c1)
+      : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// max that returns NaN if either input is NaN
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Scales CW values of this thread's tile row by alpha, casts them to
+// out_dtype (round to nearest even; NaN becomes the canonical pattern), folds
+// the largest stored |value| into the running amax (inside C only; rounding
+// is monotone, so the largest rounded value is the rounded largest value),
+// stages the warp's 32 x CW block in one of its two shared-memory buffers and
+// stores it with one TMA copy at (cx, cy, cl).
+template <int CW, int ES>
+__device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap* tm_c, float (&v)[CW], float alpha,
+                                            bool row_ok, int q0, int lane, uint8_t* stg_gen, uint32_t stg_s,
+                                            int cx, int cy, int cl, bool in_bounds, float& amax_f,
+                                            uint32_t& amax_nan) {
 #pragma unroll
-    for (int i = 0; i < PW; ++i) {
-      const float x = alpha * v[i];
-      uint32_t b = __float_as_uint(x);
-      uint32_t a = b & 0x7FFFFFFFu;
-      if (a > 0x7F800000u) {
-        b = 0x7FFFFFFFu;
-        a = 0x7FFFFFFFu;
-      }
-      w[i] = b;
-      if (row_ok && q0 + i < p.Q) amax_local = max(amax_local, a);
+  for (int i = 0; i < CW; i += 2) mul2(v[i], v[i + 1], alpha, alpha);
+  // largest |value| of the chunk inside C (NaN-propagating)
+  float m = 0.0f;
+  if (row_ok && q0 + CW <= p.Q) {
+#pragma unroll
+    for (int i = 0; i < CW; ++i) m = max_nan(m, fabsf(v[i]));
+  } else if (row_ok) {
+#pragma unroll
+    for (int i = 0; i < CW; ++i) m = max_nan(m, (q0 + i < p.Q) ? fabsf(v[i]) : 0.0f);
+  }
+  const bool has_nan = m != m;
+  if (lane == 0) ptx::bulk_wait_read_one();  // this buffer's previous store has read it
+  __syncwarp();
+  if constexpr (ES == 4) {
+    uint32_t w[CW];
+#pragma unroll
+    for (int i = 0; i < CW; ++i) {
+      const uint32_t bits = __float_as_uint(v[i]);
+      w[i] = ((bits & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FFFFFFFu : bits;
     }
+    if (!has_nan) amax_f = fmaxf(amax_f, m);
     if (!p.swap) {
 #pragma unroll
-      for (int c = 0; c < PW / 4; ++c) {
+      for (int c = 0; c < CW / 4; ++c) {
         const uint32_t off = swz((uint32_t)lane * p.out_rowbytes + c * 16u, p.out_swz_mask);
-        *reinterpret_cast<uint4*>(stg + off) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        *reinterpret_cast<uint4*>(stg_gen + off) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < PW; ++i) {
+      for (int i = 0; i < CW; ++i) {
         const uint32_t off = swz((uint32_t)i * p.out_rowbytes + lane * 4u, p.out_swz_mask);
-        *reinterpret_cast<uint32_t*>(stg + off) = w[i];
+        *reinterpret_cast<uint32_t*>(stg_gen + off) = w[i];
       }
     }
   } else {
-    uint16_t w[PW];
+    uint32_t w[CW / 2];
+    const bool bf = p.out_dtype == 1;
 #pragma unroll
-    for (int i = 0; i < PW; ++i) {
-      const float x = alpha * v[i];
-      uint16_t hb;
-      uint32_t a;
-      if (x != x) {
-        hb = 0x7FFFu;
-        a = 0x7FFFFFFFu;
-      } else if (p.out_dtype == 1) {
-        hb = __bfloat16_as_ushort(__float2bfloat16_rn(x));
-        a = ((uint32_t)hb << 16) & 0x7FFFFFFFu;
-      } else {
-        const __half hv = __float2half_rn(x);
-        hb = __half_as_ushort(hv);
-        a = __float_as_uint(__half2float(hv)) & 0x7FFFFFFFu;
+    for (int i = 0; i < CW / 2; ++i) w[i] = bf ? cvt_bf16x2(v[2 * i], v[2 * i + 1]) : cvt_f16x2(v[2 * i], v[2 * i + 1]);
+    if (has_nan) {
+#pragma unroll
+      for (int i = 0; i < CW / 2; ++i) {
+        if (v[2 * i] != v[2 * i]) w[i] = (w[i] & 0xFFFF0000u) | 0x7FFFu;
+        if (v[2 * i + 1] != v[2 * i + 1]) w[i] = (w[i] & 0x0000FFFFu) | 0x7FFF0000u;
       }
-      w[i] = hb;
-      if (row_ok && q0 + i < p.Q) amax_local = max(amax_local, a);
+    } else {
+      // the stored magnitude of the largest value, widened back to fp32
+      const float mr = bf ? __uint_as_float(cvt_bf16x2(m, 0.0f) << 16)
+                          : __half2float(__ushort_as_half((unsigned short)(cvt_f16x2(m, 0.0f) & 0xFFFFu)));
+      amax_f = fmaxf(amax_f, mr);
     }
     if (!p.swap) {
 #pragma unroll
-      for (int c = 0; c < (PW * 2) / 16; ++c) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pk[e] = (uint32_t)w[8 * c + 2 * e] | ((uint32_t)w[8 * c + 2 * e + 1] << 16);
+      for (int c = 0; c < CW / 8; ++c) {
         const uint32_t off = swz((uint32_t)lane * p.out_rowbytes + c * 16u, p.out_swz_mask);
-        *reinterpret_cast<uint4*>(stg + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(stg_gen + off) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < PW; ++i) {
+      for (int i = 0; i < CW; ++i) {
         const uint32_t off = swz((uint32_t)i * p.out_rowbytes + lane * 2u, p.out_swz_mask);
-        *reinterpret_cast<uint16_t*>(stg + off) = w[i];
+        *reinterpret_cast<uint16_t*>(stg_gen + off) = (uint16_t)((i & 1) ? (w[i / 2] >> 16) : (w[i / 2] & 0xFFFFu));
       }
     }
   }
+  if (has_nan) amax_nan = 1u;
   ptx::fence_proxy_async_smem();
   __syncwarp();
   // A box that starts inside C is clipped by the TMA unit; one that starts
-  // past its end holds nothing to store and is skipped.
-  if (lane == 0 && in_bounds) {
-    ptx::tma_store_3d(tm_c, stg_s, cx, cy, cl);
+  // past its end holds nothing to store and is skipped (no group is committed).
+  if (lane == 0) {
+    if (in_bounds) ptx::tma_store_3d(tm_c, stg_s, cx, cy, cl);
     ptx::bulk_commit();
   }
 }
 
-template <int BN, bool SLOW, bool MX>
+// Epilogue warps 0-7.  Warp w reads TMEM lanes 32*(w%4) .. +31 (the tile rows
+// it may access) and the columns of half w/4.  Per work unit: (slow) promote
+// each 128-K chunk into fp32 registers; (split-K) publish the partial tile and
+// let the last arrival finish it; then scale, cast, amax and store.
+template <int BN, bool SLOW, int CG, int CW, int ES>
+__device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm_c, uint8_t* sgen, uint32_t sbase,
+                                         uint32_t tmem_base, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t bar_epi,
+                                         volatile uint32_t* misc, volatile uint32_t* abort_flag, uint32_t rank,
+                                         long long u_first, long long u_step, int warp, int lane) {
+  constexpr int H0 = half0_cols(BN);
+  constexpr int HMAX = H0;                    // widest column range of a warp
+  constexpr int LDW = HMAX < 32 ? HMAX : 32;  // columns per tcgen05.ld while promoting
+  static_assert(!SLOW || H0 * 2 == BN, "slow accumulation splits the tile evenly");
+  static_assert(H0 % CW == 0 && (BN - H0) % CW == 0, "chunks tile each half");
+  const int qd = warp & 3;
+  const int h = warp >> 2;
+  const int row = qd * 32 + lane;
+  const int col0 = h ? H0 : 0;
+  const int ncols = h ? BN - H0 : H0;
+  const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+  uint32_t abuf = 0, aphase = 0, epi_phase = 0;
+  float amax_f = 0.0f;
+  uint32_t amax_nan = 0u;
+  bool ok = true;
+  const float alpha = p.sa_tensor ? (__ldg(p.sa_tensor) * __ldg(p.sb_tensor)) : 1.0f;
+  float* ys_w = reinterpret_cast<float*>(sgen + p.off_ys) + warp * HMAX;
+  uint8_t* stg = sgen + p.off_out + warp * kStageOutBytes;
+  const uint32_t stg_s = sbase + p.off_out + warp * kStageOutBytes;
+  uint32_t stg_sel = 0;
+  float acc[SLOW ? HMAX : 1];  // slow accumulation: fp32 running sum of the promoted chunks
+  (void)acc;
+  (void)ys_w;
+  // The pair leader's accumulator-empty barrier collects both CTAs' warps.
+  const uint32_t tempty_target = (CG == 2) ? ptx::mapa_shared(bar_tempty, 0u) : bar_tempty;
+  auto release_acc = [&]() {
+    ptx::tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (CG == 2)
+        ptx::mbar_arrive_cluster(tempty_target + 8u * abuf);
+      else
+        ptx::mbar_arrive(bar_tempty + 8u * abuf);
+    }
+    if (p.num_acc == 2) {
+      abuf ^= 1u;
+      if (abuf == 0) aphase ^= 1u;
+    } else {
+      aphase ^= 1u;
+    }
+  };
+
+  for (long long u = u_first; ok && u < p.units; u += u_step) {
+    const Unit t = decode_unit(u, p);
+    const int xbase = t.tr * kBlockM * CG + (int)rank * kBlockM;  // first X row of this CTA's half
+    const int xr = xbase + row;                                   // row of X this thread owns
+    const bool row_ok = xr < p.R;
+    if constexpr (SLOW) {
+      // One hand-off per 128-K chunk: acc += s_x(row, c) * s_y(col, c) * chunk.
+      for (int g = 0; g < t.kb1 - t.kb0; ++g) {
+        float xs = 1.0f, yb = 1.0f;
+        if (p.x_kind != kScaleNone) {
+          const int c = t.kb0 + g;
+          if (row_ok) {
+            xs = (p.x_kind == kScaleRow)
+                     ? __ldg(p.x_scale + ((size_t)t.l * p.R + xr) * p.scale_kb + c)
+                     : __ldg(p.x_scale + ((size_t)t.l * ((p.R + 127) / 128) + xr / 128) * p.scale_kb + c);
+          }
+          if (p.y_kind == kScaleBlock128) {
+            // BN divides 128 and tiles start at multiples of BN: one scale per tile and chunk
+            const int yq = t.tq * BN;
+            yb = (yq < p.Q) ? __ldg(p.y_scale + ((size_t)t.l * ((p.Q + 127) / 128) + yq / 128) * p.scale_kb + c)
+                            : 0.0f;
+          } else {
+            __syncwarp();
+            for (int j = lane; j < ncols; j += 32) {
+              const int yq = t.tq * BN + col0 + j;
+              ys_w[j] = (yq < p.Q) ? __ldg(p.y_scale + ((size_t)t.l * p.Q + yq) * p.scale_kb + c) : 0.0f;
+            }
+            __syncwarp();
+          }
+        }
+        if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, kErrEpiAcc)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after_sync();
+        const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
+        const float f = xs * yb;
+#pragma unroll
+        for (int pc = 0; pc < HMAX / LDW; ++pc) {
+          uint32_t r[LDW];
+          tmem_load<LDW>(taddr + pc * LDW, r);
+#pragma unroll
+          for (int i = 0; i < LDW; i += 2) {
+            const int j = pc * LDW + i;
+            const float v0 = __uint_as_float(r[i]), v1 = __uint_as_float(r[i + 1]);
+            if (g == 0) {
+              acc[j] = v0;
+              acc[j + 1] = v1;
+              if (p.x_kind != kScaleNone) {
+                if (p.y_kind == kScaleBlock128)
+                  mul2(acc[j], acc[j + 1], f, f);
+                else
+                  mul2(acc[j], acc[j + 1], xs * ys_w[j], xs * ys_w[j + 1]);
+              }
+            } else if (p.x_kind == kScaleNone) {
+              add2(acc[j], acc[j + 1], v0, v1);
+            } else if (p.y_kind == kScaleBlock128) {
+              fma2(acc[j], acc[j + 1], f, f, v0, v1);
+            } else {
+              fma2(acc[j], acc[j + 1], xs * ys_w[j], xs * ys_w[j + 1], v0, v1);
+            }
+          }
+        }
+        release_acc();
+      }
+      if (!ok) break;
+    } else {
+      if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, kErrEpiAcc)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after_sync();
+    }
+    // Fast accumulation reads the finished tile from TMEM chunk by chunk.
+    const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
+    auto get_chunk = [&](int ci, float(&v)[CW]) {
+      if constexpr (SLOW) {
+#pragma unroll
+        for (int i = 0; i < CW; ++i) v[i] = acc[ci * CW + i];
+      } else {
+        uint32_t r[CW];
+        tmem_load<CW>(taddr + ci * CW, r);
+#pragma unroll
+        for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
+      }
+    };
+    constexpr int NCH_MAX = HMAX / CW;
+    const int nch = ncols / CW;
+
+    // ---------------------------------------------------- split-K fix-up
+    bool finish = true;
+    float* tile_ws = nullptr;
+    if (p.splits > 1) {
+      const long long tile = (((long long)t.l * p.tiles_r + t.tr) * p.tiles_q + t.tq) * CG + rank;
+      tile_ws = p.ws_partials + (size_t)tile * p.splits * (kBlockM * BN);
+      float* slot = tile_ws + (size_t)t.s * (kBlockM * BN);
+#pragma unroll
+      for (int ci = 0; ci < NCH_MAX; ++ci) {
+        if (ci < nch) {
+          float v[CW];
+          get_chunk(ci, v);
+#pragma unroll
+          for (int i = 0; i < CW; ++i) __stcg(slot + (size_t)(col0 + ci * CW + i) * kBlockM + row, v[i]);
+        }
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_epi);
+      if (!wait_bar(bar_epi, epi_phase, abort_flag, kErrEpiSync)) {
+        ok = false;
+        break;
+      }
+      epi_phase ^= 1u;
+      if (warp == 0 && lane == 0) {
+        __threadfence();
+        misc[2] = atomicAdd(p.ws_counters + tile, 1u);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_epi);
+      if (!wait_bar(bar_epi, epi_phase, abort_flag, kErrEpiSync)) {
+        ok = false;
+        break;
+      }
+      epi_phase ^= 1u;
+      finish = misc[2] == (uint32_t)(p.splits - 1);  // the last arrival finishes the tile
+      if (finish) __threadfence();
+    }
+
+    // ---------------------------------------------------- scale, cast, store
+    if (finish) {
+      const int r0 = xbase + qd * 32;  // X row of the warp's first lane
+#pragma unroll
+      for (int ci = 0; ci < NCH_MAX; ++ci) {
+        if (ci < nch) {
+          float v[CW];
+          get_chunk(ci, v);
+          if (p.splits > 1) {
+            // Partials are added in split order 0..S-1 whichever CTA arrived last.
+#pragma unroll
+            for (int i = 0; i < CW; ++i) {
+              const size_t off = (size_t)(col0 + ci * CW + i) * kBlockM + row;
+              float sum = (t.s == 0) ? v[i] : __ldcg(tile_ws + off);
+              for (int ss = 1; ss < p.splits; ++ss)
+                sum += (ss == t.s) ? v[i] : __ldcg(tile_ws + (size_t)ss * (kBlockM * BN) + off);
+              v[i] = sum;
+            }
+          }
+          const int q0 = t.tq * BN + col0 + ci * CW;  // Y row of the chunk's first column
+          store_chunk<CW, ES>(p, tm_c, v, alpha, row_ok, q0, lane, stg + stg_sel * (kStageOutBytes / 2),
+                              stg_s + stg_sel * (kStageOutBytes / 2), p.swap ? r0 : q0, p.swap ? q0 : r0, t.l,
+                              q0 < p.Q && r0 < p.R, amax_f, amax_nan);
+          stg_sel ^= 1u;
+        }
+      }
+    }
+    if constexpr (!SLOW) release_acc();
+  }
+  if (lane == 0) ptx::bulk_wait_all();
+  uint32_t amax_local = amax_nan ? 0x7FFFFFFFu : __float_as_uint(amax_f);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax_local = max(amax_local, __shfl_xor_sync(0xFFFFFFFFu, amax_local, o));
+  if (lane == 0 && amax_local != 0u) atomicMax(p.amax_bits, amax_local);
+}
+
+template <int BN, bool SLOW, bool MX, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8mm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                  const __grid_constant__ CUtensorMap tm_c, const KParams p) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(!MX || BN >= 128, "MX tiles cover whole 128-row scale-factor atoms");
   static_assert(!SLOW || BN <= 128, "slow accumulation keeps BN/2 fp32 sums per thread in registers");
+  static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
+  static_assert(!MX || CG == 1, "the block-scaled form runs on single-CTA tiles");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sraw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (sraw + 1023u) & ~1023u;
@@ -268,6 +531,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
+  // CG == 2: a cluster of two CTAs computes 256-row tiles with two-SM MMAs
+  // issued by the leader (rank 0); each CTA stages its own 128 rows of X and
+  // half of the Y tile, and holds its 128 rows of the accumulator in TMEM.
+  const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0u;
+  const long long u_first = blockIdx.x / CG;
+  const long long u_step = gridDim.x / CG;
 
   const uint32_t bar_full = sbase + p.off_bar;
   const uint32_t bar_empty = bar_full + 8u * S;
@@ -285,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(bar_tfull + 8u * b, 1);
-      ptx::mbar_init(bar_tempty + 8u * b, kEpiWarps);
+      ptx::mbar_init(bar_tempty + 8u * b, kEpiWarps * CG);  // the pair's epilogue warps arrive on the leader
     }
     ptx::mbar_init(bar_epi, kEpiWarps);
     ptx::mbar_init(bar_done, 1);
@@ -294,11 +564,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(misc)), p.tmem_cols);
-    ptx::tmem_relinquish();
+    if constexpr (CG == 2) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(const_cast<uint32_t*>(misc)), p.tmem_cols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(misc)), p.tmem_cols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CG == 2)
+    ptx::cluster_sync();  // both CTAs' barriers exist before either signals the other
+  else
+    __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem_base = misc[0];
   volatile uint32_t* abort_flag = misc + 1;
@@ -309,20 +587,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       long long narm = 0;
       bool ok = true;
-      const uint32_t tx = p.x_stage_bytes + p.y_stage_bytes + (MX ? 512u * (1 + p.sfy_atoms) : 0u);
-      for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+      // With a CTA pair both CTAs' copies complete on the leader's full barrier,
+      // which the leader arms with the bytes of both.
+      const uint32_t tx = CG * (p.x_stage_bytes + p.y_stage_bytes) + (MX ? 512u * (1 + p.sfy_atoms) : 0u);
+      for (long long u = u_first; ok && u < p.units; u += u_step) {
         const Unit t = decode_unit(u, p);
+        const int xrow0 = t.tr * kBlockM * CG + (int)rank * kBlockM;
+        const int yrow0 = t.tq * BN + (int)rank * (BN / CG);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!wait_bar(bar_empty + 8u * stage, phase ^ 1u, abort_flag, kErrProducer)) {
             ok = false;
             break;
           }
           const uint32_t fb = bar_full + 8u * stage;
-          ptx::mbar_arrive_expect_tx(fb, tx);
-          ptx::tma_load_3d(sbase + p.off_x + stage * p.x_stage_bytes, &tm_x, fb, kb * kBlockK,
-                           t.tr * kBlockM, t.l);
-          ptx::tma_load_3d(sbase + p.off_y + stage * p.y_stage_bytes, &tm_y, fb, kb * kBlockK,
-                           t.tq * BN, t.l);
+          if constexpr (CG == 2) {
+            const uint32_t fb_leader = ptx::mapa_shared(fb, 0u);
+            if (leader) ptx::mbar_arrive_expect_tx(fb, tx);
+            ptx::tma_load_3d_pair(sbase + p.off_x + stage * p.x_stage_bytes, &tm_x, fb_leader, kb * kBlockK, xrow0,
+                                  t.l);
+            ptx::tma_load_3d_pair(sbase + p.off_y + stage * p.y_stage_bytes, &tm_y, fb_leader, kb * kBlockK, yrow0,
+                                  t.l);
+          } else {
+            ptx::mbar_arrive_expect_tx(fb, tx);
+            ptx::tma_load_3d(sbase + p.off_x + stage * p.x_stage_bytes, &tm_x, fb, kb * kBlockK, xrow0, t.l);
+            ptx::tma_load_3d(sbase + p.off_y + stage * p.y_stage_bytes, &tm_y, fb, kb * kBlockK, yrow0, t.l);
+          }
           if constexpr (MX) {
             const uint32_t sf = sbase + p.off_sf + stage * p.sf_stage_bytes;
             const uint8_t* gx =
@@ -345,17 +634,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Wait until every copy this thread started has landed (all of them
       // were consumed already unless another role aborted).
       // (stage, phase) is the next slot: slots below it were last armed in
-      // this pass of the ring, the others in the previous pass.
-      for (int s = 0; s < S; ++s) {
-        if (narm > s) drain_wait(bar_full + 8u * s, ((uint32_t)s < stage) ? phase : (phase ^ 1u));
+      // this pass of the ring, the others in the previous pass.  With a CTA
+      // pair the leader's barriers also track the peer's copies.
+      if (leader) {
+        for (int s = 0; s < S; ++s) {
+          if (narm > s) drain_wait(bar_full + 8u * s, ((uint32_t)s < stage) ? phase : (phase ^ 1u));
+        }
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
       bool ok = true;
-      for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+      for (long long u = u_first; ok && u < p.units; u += u_step) {
         const Unit t = decode_unit(u, p);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           const bool gstart = SLOW || kb == t.kb0;
@@ -389,14 +681,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::mma_mxf8f6f4(d, adesc + 2u * k, bdesc + 2u * k, idesc, sf_x, sf_y,
                                 (!gstart || k > 0) ? 1u : 0u);
             }
+          } else if constexpr (CG == 2) {
+#pragma unroll
+            for (int k = 0; k < kBlockK / kUmmaK; ++k)
+              ptx::mma_f8f6f4_pair(d, adesc + 2u * k, bdesc + 2u * k, p.idesc, (!gstart || k > 0) ? 1u : 0u);
           } else {
 #pragma unroll
             for (int k = 0; k < kBlockK / kUmmaK; ++k)
               ptx::mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, p.idesc, (!gstart || k > 0) ? 1u : 0u);
           }
-          ptx::tc_commit(bar_empty + 8u * stage);
+          if constexpr (CG == 2)
+            ptx::tc_commit_pair(bar_empty + 8u * stage, (uint16_t)0x3);
+          else
+            ptx::tc_commit(bar_empty + 8u * stage);
           if (gend) {
-            ptx::tc_commit(bar_tfull + 8u * abuf);
+            if constexpr (CG == 2)
+              ptx::tc_commit_pair(bar_tfull + 8u * abuf, (uint16_t)0x3);
+            else
+              ptx::tc_commit(bar_tfull + 8u * abuf);
             if (p.num_acc == 2) {
               abuf ^= 1u;
               if (abuf == 0) aphase ^= 1u;
@@ -411,196 +713,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Drain: every MMA issued above has completed before TMEM is freed.
-      ptx::tc_commit(bar_done);
+      if constexpr (CG == 2)
+        ptx::tc_commit_pair(bar_done, (uint16_t)0x1);
+      else
+        ptx::tc_commit(bar_done);
       drain_wait(bar_done, 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    constexpr int HALF = BN / 2;
-    constexpr int PW = HALF < 16 ? HALF : 16;  // columns per output piece
-    constexpr int NPC = HALF / PW;
-    constexpr int LDW = HALF < 32 ? HALF : 32;  // columns per tcgen05.ld while promoting
-    const int qd = warp & 3;                    // TMEM lane quarter this warp may access
-    const int h = warp >> 2;                    // column half
-    const int row = qd * 32 + lane;             // tile row == TMEM lane
-    const int col0 = h * HALF;
-    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-    uint32_t abuf = 0, aphase = 0, epi_phase = 0;
-    uint32_t amax_local = 0;
-    bool ok = true;
-    const float alpha = p.sa_tensor ? (__ldg(p.sa_tensor) * __ldg(p.sb_tensor)) : 1.0f;
-    float* ys_w = reinterpret_cast<float*>(sgen + p.off_ys) + warp * HALF;
-    uint8_t* stg = sgen + p.off_out + warp * kStageOutBytes;
-    const uint32_t stg_s = sbase + p.off_out + warp * kStageOutBytes;
-    float acc[SLOW ? HALF : 1];  // slow accumulation: fp32 running sum of the promoted chunks
-    (void)acc;
-    (void)ys_w;
-
-    for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-      const Unit t = decode_unit(u, p);
-      const int xr = t.tr * kBlockM + row;  // row of X this thread owns
-      const bool row_ok = xr < p.R;
-      if constexpr (SLOW) {
-        // One hand-off per 128-K chunk: acc += s_x(row, c) * s_y(col, c) * chunk.
-        for (int g = 0; g < t.kb1 - t.kb0; ++g) {
-          float xs = 1.0f;
-          if (p.x_kind != kScaleNone) {
-            const int c = t.kb0 + g;
-            if (row_ok) {
-              xs = (p.x_kind == kScaleRow)
-                       ? __ldg(p.x_scale + ((size_t)t.l * p.R + xr) * p.scale_kb + c)
-                       : __ldg(p.x_scale + ((size_t)t.l * ((p.R + 127) / 128) + xr / 128) * p.scale_kb + c);
-            }
-            __syncwarp();
-            for (int j = lane; j < HALF; j += 32) {
-              const int yq = t.tq * BN + col0 + j;
-              float v = 0.0f;
-              if (yq < p.Q) {
-                v = (p.y_kind == kScaleRow)
-                        ? __ldg(p.y_scale + ((size_t)t.l * p.Q + yq) * p.scale_kb + c)
-                        : __ldg(p.y_scale + ((size_t)t.l * ((p.Q + 127) / 128) + yq / 128) * p.scale_kb + c);
-              }
-              ys_w[j] = v;
-            }
-            __syncwarp();
-          }
-          if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, kErrEpiAcc)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after_sync();
-          const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
-#pragma unroll
-          for (int pc = 0; pc < HALF / LDW; ++pc) {
-            uint32_t r[LDW];
-            tmem_load<LDW>(taddr + pc * LDW, r);
-#pragma unroll
-            for (int i = 0; i < LDW; ++i) {
-              const int j = pc * LDW + i;
-              const float v = __uint_as_float(r[i]);
-              if (p.x_kind != kScaleNone) {
-                const float f = xs * ys_w[j];
-                acc[j] = (g == 0) ? f * v : fmaf(f, v, acc[j]);
-              } else {
-                acc[j] = (g == 0) ? v : acc[j] + v;
-              }
-            }
-          }
-          ptx::tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar_tempty + 8u * abuf);
-          if (p.num_acc == 2) {
-            abuf ^= 1u;
-            if (abuf == 0) aphase ^= 1u;
-          } else {
-            aphase ^= 1u;
-          }
-        }
-        if (!ok) break;
-      } else {
-        if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, kErrEpiAcc)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after_sync();
-      }
-      // Fast accumulation reads the finished tile from TMEM piece by piece.
-      const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
-      auto get_piece = [&](int pc, float(&v)[PW]) {
-        if constexpr (SLOW) {
-#pragma unroll
-          for (int i = 0; i < PW; ++i) v[i] = acc[pc * PW + i];
-        } else {
-          uint32_t r[PW];
-          tmem_load<PW>(taddr + pc * PW, r);
-#pragma unroll
-          for (int i = 0; i < PW; ++i) v[i] = __uint_as_float(r[i]);
-        }
-      };
-
-      // ---------------------------------------------------- split-K fix-up
-      bool finish = true;
-      float* tile_ws = nullptr;
-      if (p.splits > 1) {
-        const long long tile = ((long long)t.l * p.tiles_r + t.tr) * p.tiles_q + t.tq;
-        tile_ws = p.ws_partials + (size_t)tile * p.splits * (kBlockM * BN);
-        float* slot = tile_ws + (size_t)t.s * (kBlockM * BN);
-#pragma unroll
-        for (int pc = 0; pc < NPC; ++pc) {
-          float v[PW];
-          get_piece(pc, v);
-#pragma unroll
-          for (int i = 0; i < PW; ++i) __stcg(slot + (size_t)(col0 + pc * PW + i) * kBlockM + row, v[i]);
-        }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_epi);
-        if (!wait_bar(bar_epi, epi_phase, abort_flag, kErrEpiSync)) {
-          ok = false;
-          break;
-        }
-        epi_phase ^= 1u;
-        if (warp == 0 && lane == 0) {
-          __threadfence();
-          misc[2] = atomicAdd(p.ws_counters + tile, 1u);
-        }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_epi);
-        if (!wait_bar(bar_epi, epi_phase, abort_flag, kErrEpiSync)) {
-          ok = false;
-          break;
-        }
-        epi_phase ^= 1u;
-        finish = misc[2] == (uint32_t)(p.splits - 1);  // the last arrival finishes the tile
-        if (finish) __threadfence();
-      }
-
-      // ---------------------------------------------------- scale, cast, store
-      if (finish) {
-#pragma unroll
-        for (int pc = 0; pc < NPC; ++pc) {
-          float v[PW];
-          get_piece(pc, v);
-          if (p.splits > 1) {
-            // Partials are added in split order 0..S-1 whichever CTA arrived last.
-#pragma unroll
-            for (int i = 0; i < PW; ++i) {
-              const size_t off = (size_t)(col0 + pc * PW + i) * kBlockM + row;
-              float sum = (t.s == 0) ? v[i] : __ldcg(tile_ws + off);
-              for (int ss = 1; ss < p.splits; ++ss)
-                sum += (ss == t.s) ? v[i] : __ldcg(tile_ws + (size_t)ss * (kBlockM * BN) + off);
-              v[i] = sum;
-            }
-          }
-          const int q0 = t.tq * BN + col0 + pc * PW;  // Y row of the piece's first column
-          const int r0 = t.tr * kBlockM + qd * 32;    // X row of the warp's first lane
-          store_piece<PW>(p, &tm_c, v, alpha, row_ok, q0, lane, stg, stg_s, p.swap ? r0 : q0,
-                          p.swap ? q0 : r0, t.l, q0 < p.Q && r0 < p.R, amax_local);
-        }
-      }
-      if constexpr (!SLOW) {
-        ptx::tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_tempty + 8u * abuf);
-        if (p.num_acc == 2) {
-          abuf ^= 1u;
-          if (abuf == 0) aphase ^= 1u;
-        } else {
-          aphase ^= 1u;
-        }
-      }
-    }
-    if (lane == 0) ptx::bulk_wait_all();
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax_local = max(amax_local, __shfl_xor_sync(0xFFFFFFFFu, amax_local, o));
-    if (lane == 0 && amax_local != 0u) atomicMax(p.amax_bits, amax_local);
+    if (p.out_es == 4)
+      epilogue<BN, SLOW, CG, chunk_cols(BN, 4), 4>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty, bar_epi,
+                                                    misc, abort_flag, rank, u_first, u_step, warp, lane);
+    else
+      epilogue<BN, SLOW, CG, chunk_cols(BN, 2), 2>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty, bar_epi,
+                                                    misc, abort_flag, rank, u_first, u_step, warp, lane);
   }
 
   ptx::tc_fence_before_sync();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    ptx::tc_fence_after_sync();
-    ptx::tmem_dealloc(tmem_base, p.tmem_cols);
+  if constexpr (CG == 2) {
+    // Neither CTA leaves (or frees TMEM) while the pair's MMAs or copies may
+    // still touch its shared memory or TMEM.
+    ptx::cluster_sync();
+    if (warp == kMmaWarp) {
+      ptx::tc_fence_after_sync();
+      ptx::tmem_dealloc_pair(tmem_base, p.tmem_cols);
+    }
+  } else {
+    __syncthreads();
+    if (warp == kMmaWarp) {
+      ptx::tc_fence_after_sync();
+      ptx::tmem_dealloc(tmem_base, p.tmem_cols);
+    }
   }
 }
 

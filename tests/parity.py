@@ -41,14 +41,15 @@ def to_device(p: synth.Problem, device="cuda:0"):
     return (p.a.to(dev), p.b.to(dev), p.scale_a.to(dev), p.scale_b.to(dev))
 
 
-def run_gpu(p: synth.Problem, *, splitk=0, swap_ab=0, block_n=0, device="cuda:0", tensors=None):
+def run_gpu(p: synth.Problem, *, splitk=0, swap_ab=0, block_n=0, cta_pair=0, device="cuda:0", tensors=None):
     """One fp8mm_run through the C ABI; returns (C on device [L][M][N], amax tensor, plan)."""
     a, b, sa, sb = tensors if tensors is not None else to_device(p, device)
     c, amax = pm.scaled_mm(a, b, sa, sb, out_dtype=synth.OUT_TORCH[p.out_dtype],
                            use_fast_accum=p.fast_accum, a_fmt=p.a_fmt, b_fmt=p.b_fmt,
-                           scale_mode=p.scale_mode, splitk=splitk, swap_ab=swap_ab, block_n=block_n)
+                           scale_mode=p.scale_mode, splitk=splitk, swap_ab=swap_ab, block_n=block_n,
+                           cta_pair=cta_pair)
     key = (p.M, p.N, p.K, p.L, p.a_fmt, p.b_fmt, p.scale_mode, p.out_dtype, 1 if p.fast_accum else 0,
-           splitk, swap_ab, block_n, torch.device(device).index or 0)
+           splitk, swap_ab, block_n, torch.device(device).index or 0, cta_pair)
     return c, amax, pm.plan_for(key)
 
 
@@ -97,8 +98,7 @@ def check(p: synth.Problem, c: torch.Tensor, amax: torch.Tensor, *, rows=None, o
             assert np.array_equal(np.isnan(got[nf]), np.isnan(co[nf])), "NaN positions differ"
             inf_or = np.isinf(co[nf])
             assert np.array_equal(got[nf][inf_or], co[nf][inf_or]), "Inf signs differ"
-            # a finite oracle value may not become non-finite on the GPU
-        assert not (finite & ~np.isfinite(got)).any() or True
+        # (a finite oracle value that became non-finite on the GPU fails the bound above)
         nan_mask = torch.isnan(got_t.float())
         if nan_mask.any():
             ib = got_t.view(torch.int32 if p.out_dtype == synth.OUT_F32 else torch.int16)

@@ -164,3 +164,29 @@ def test_launch_count_is_one_kernel():
     p = synth.llm_per_tensor(M=256, N=256, K=256, seed=23)
     _, _, plan = run_gpu(p)
     assert plan.kernel_launches() == 1
+
+
+@pytest.mark.parametrize("fast,block_n", [(True, 256), (True, 128), (False, 128)])
+def test_cta_pair_tiles_ragged(fast, block_n):
+    # two-SM MMAs: 256-row tiles split over a CTA pair, ragged in M, N and K
+    p = synth.llm_per_tensor(M=520, N=392, K=640, seed=24, fast_accum=fast)
+    c, amax, plan = _run_check(p, block_n=block_n, cta_pair=1, swap_ab=2)
+    assert plan.info()["cta_pair"] == 1
+
+
+def test_cta_pair_blockwise_and_split_k():
+    p = synth.blockwise(M=384, N=264, K=1024, seed=25)
+    c, amax, plan = _run_check(p, cta_pair=1, splitk=3, swap_ab=2)
+    assert plan.info()["cta_pair"] == 1 and plan.info()["splitk"] == 3
+
+
+def test_cta_pair_matches_single_cta_within_bound():
+    p = synth.llm_per_tensor(M=512, N=512, K=1024, seed=26, fast_accum=True)
+    t = to_device(p)
+    c1, a1, pl1 = run_gpu(p, tensors=t, cta_pair=1, block_n=256)
+    c1 = c1.clone()
+    c2, a2, pl2 = run_gpu(p, tensors=t, cta_pair=2, block_n=256)
+    torch.cuda.synchronize()
+    assert pl1.info()["cta_pair"] == 1 and pl2.info()["cta_pair"] == 0
+    check(p, c1, a1)
+    check(p, c2, a2)
