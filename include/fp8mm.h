@@ -93,10 +93,12 @@ typedef struct {
                           128-K chunk (their scales change per chunk). */
   int32_t splitk;      /* 0: choose; S >= 1: split K into S contiguous 128-aligned ranges */
   int32_t swap_ab;     /* 0: choose; 1: force on; 2: force off */
-  int32_t block_n;     /* 0: choose; else the tile width on the MMA's N side (16..256) */
+  int32_t block_n;     /* 0: choose; else the tile width on the MMA's N side (a multiple of
+                          16 from 16 to 256 that the library instantiates) */
   int32_t device;      /* CUDA device ordinal the plan is for */
   int32_t cta_pair;    /* two-SM (CTA pair) tiles: 0 choose; 1 force on; 2 force off */
-  int32_t reserved[2]; /* must be 0 */
+  int32_t epi_warps;   /* epilogue warps per CTA: 0 choose, 8 or 16 */
+  int32_t stages;      /* shared-memory pipeline depth: 0 choose (as many as fit), else 2..12 */
 } fp8mm_desc;
 
 typedef struct fp8mm_plan_s fp8mm_plan_t;
@@ -113,6 +115,7 @@ typedef struct {
   int32_t slow;         /* 1 if 128-K chunks are promoted in registers */
   int32_t smem_bytes;   /* dynamic shared memory per CTA */
   int32_t cta_pair;     /* 1 if tiles are computed by CTA pairs with two-SM MMAs (256-row tiles) */
+  int32_t epi_warps;    /* epilogue warps per CTA */
 } fp8mm_plan_info;
 
 /* Validate desc and choose tiles, swap-AB and split-K for the device.  On

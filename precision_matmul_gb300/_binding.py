@@ -33,14 +33,14 @@ class fp8mm_desc(ctypes.Structure):
                 ("a_fmt", ctypes.c_int32), ("b_fmt", ctypes.c_int32), ("scale_mode", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("fast_accum", ctypes.c_int32), ("splitk", ctypes.c_int32),
                 ("swap_ab", ctypes.c_int32), ("block_n", ctypes.c_int32), ("device", ctypes.c_int32),
-                ("cta_pair", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
+                ("cta_pair", ctypes.c_int32), ("epi_warps", ctypes.c_int32), ("stages", ctypes.c_int32)]
 
 
 class fp8mm_plan_info(ctypes.Structure):
     _fields_ = [("swap_ab", ctypes.c_int32), ("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("splitk", ctypes.c_int32), ("stages", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("units", ctypes.c_int64), ("slow", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("cta_pair", ctypes.c_int32)]
+                ("cta_pair", ctypes.c_int32), ("epi_warps", ctypes.c_int32)]
 
 
 class FP8MMError(RuntimeError):
@@ -99,13 +99,15 @@ def _check(st: int, where: str):
 
 def make_desc(M, N, K, L=1, *, a_fmt=FP8MM_E4M3, b_fmt=FP8MM_E4M3, scale_mode=FP8MM_SCALE_TENSOR,
               out_dtype=FP8MM_OUT_BF16, fast_accum=1, splitk=0, swap_ab=0, block_n=0, device=0,
-              cta_pair=0) -> fp8mm_desc:
+              cta_pair=0, epi_warps=0, stages=0) -> fp8mm_desc:
     d = fp8mm_desc()
     d.M, d.N, d.K, d.L = int(M), int(N), int(K), int(L)
     d.a_fmt, d.b_fmt, d.scale_mode, d.out_dtype = int(a_fmt), int(b_fmt), int(scale_mode), int(out_dtype)
     d.fast_accum, d.splitk, d.swap_ab, d.block_n, d.device = (int(fast_accum), int(splitk), int(swap_ab),
                                                               int(block_n), int(device))
     d.cta_pair = int(cta_pair)
+    d.epi_warps = int(epi_warps)
+    d.stages = int(stages)
     return d
 
 

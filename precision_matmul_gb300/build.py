@@ -14,8 +14,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfp8mm.so")
-SOURCES = ["fp8mm_host.cu"]
-HEADERS = ["fp8mm_kernel.cuh", "ptx.cuh"]
+SOURCES = ["fp8mm_host.cu", "fp8mm_inst_narrow.cu", "fp8mm_inst_fast128.cu", "fp8mm_inst_fast256.cu",
+           "fp8mm_inst_pair.cu", "fp8mm_inst_slow.cu", "fp8mm_inst_mx.cu", "fp8mm_inst_mx_wide.cu"]
+HEADERS = ["fp8mm_kernel.cuh", "fp8mm_kernels.h", "ptx.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -36,17 +37,30 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every translation unit in parallel, then link the shared library."""
     if not force and not _stale():
         return LIB
+    from concurrent.futures import ThreadPoolExecutor
     os.makedirs(BUILD, exist_ok=True)
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), "-std=c++17", "-O3", ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
-           "-I" + os.path.join(ROOT, "include"), "-I" + CSRC,
-           *[os.path.join(CSRC, s) for s in SOURCES], "-o", tmp]
+    nvcc = nvcc_path()
+    common = ["-std=c++17", "-O3", ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
+              "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+        common.insert(0, "-Xptxas=-v")
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + f".{os.getpid()}.o")
+        subprocess.run([nvcc, *common, "-c", os.path.join(CSRC, src), "-o", obj], check=True)
+        return obj
+
+    workers = max(1, min(len(SOURCES), os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = LIB + f".tmp{os.getpid()}"
+    subprocess.run([nvcc, ARCH, "-shared", *objs, "-o", tmp], check=True)
     os.replace(tmp, LIB)
+    for o in objs:
+        os.remove(o)
     return LIB
 
 

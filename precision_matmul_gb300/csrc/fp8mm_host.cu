@@ -11,16 +11,19 @@
 #include <new>
 
 #include "fp8mm.h"
-#include "fp8mm_kernel.cuh"
+#include "fp8mm_kernels.h"
 
 using namespace fp8mm;
+
+// Device word recording aborted waits; kernels receive its address.
+__device__ unsigned g_fp8mm_abort_word = 0u;
 
 struct fp8mm_plan_s {
   fp8mm_desc d;
   int sms = 0;
   int max_smem = 0;
   int swap = 0, bn = 0, splits = 1, kb_per_split = 0, num_kb = 0, stages = 0, num_acc = 2;
-  int group = 1, slow = 0, mx = 0, out_es = 4, cg = 1;
+  int group = 1, slow = 0, mx = 0, out_es = 4, cg = 1, ew = 8;
   int64_t R = 0, Q = 0;
   int tiles_r = 0, tiles_q = 0;
   long long units = 0;
@@ -34,40 +37,6 @@ struct fp8mm_plan_s {
 };
 
 namespace {
-
-using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const KParams);
-
-template <int BN, bool SLOW, bool MX, int CG = 1>
-KernelFn kfn() {
-  return &fp8mm_kernel<BN, SLOW, MX, CG>;
-}
-
-// Instantiated kernels.  Pair (two-SM) tiles: 256 x 256 for fast accumulation
-// and 256 x 128 for slow accumulation (whose promotion keeps BN/2 sums per
-// thread in registers); single-CTA tiles for everything else.
-KernelFn select_kernel(int bn, bool slow, bool mx, int cg) {
-  if (cg == 2) {
-    if (mx) return nullptr;
-    if (bn == 256 && !slow) return kfn<256, false, false, 2>();
-    if (bn == 128) return slow ? kfn<128, true, false, 2>() : kfn<128, false, false, 2>();
-    return nullptr;
-  }
-  if (mx) {
-    switch (bn) {
-      case 128: return slow ? kfn<128, true, true>() : kfn<128, false, true>();
-      case 256: return slow ? nullptr : kfn<256, false, true>();
-      default: return nullptr;
-    }
-  }
-  switch (bn) {
-    case 16: return slow ? kfn<16, true, false>() : kfn<16, false, false>();
-    case 32: return slow ? kfn<32, true, false>() : kfn<32, false, false>();
-    case 64: return slow ? kfn<64, true, false>() : kfn<64, false, false>();
-    case 128: return slow ? kfn<128, true, false>() : kfn<128, false, false>();
-    case 256: return slow ? nullptr : kfn<256, false, false>();
-    default: return nullptr;
-  }
-}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
@@ -94,22 +63,38 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int out_size(int out_dtype) { return out_dtype == FP8MM_OUT_F32 ? 4 : 2; }
 
-// Per-device, per-kernel opt-in to large dynamic shared memory.
+// Device address of the abort word, looked up once per device (the current
+// device must be `device`).
+unsigned* abort_word_address(int device) {
+  static std::mutex mu;
+  static unsigned* addr[64] = {};
+  if (device < 0 || device >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[device]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fp8mm_abort_word) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[device] = static_cast<unsigned*>(p);
+  }
+  return addr[device];
+}
+
+// Per-device, per-kernel opt-in to the device's full dynamic shared memory.
 cudaError_t ensure_smem_attr(KernelFn fn, int device, size_t bytes) {
   static std::mutex mu;
-  static const void* done[64][16] = {};
+  static const void* done[64][32] = {};
   std::lock_guard<std::mutex> lk(mu);
   if (device >= 0 && device < 64) {
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 32; ++i) {
       if (done[device][i] == (const void*)fn) return cudaSuccess;
     }
   }
-  // Opt in to the device's full limit once, so that any later plan of the
-  // same kernel (another stage count or layout) fits as well.
   cudaError_t e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   if (device >= 0 && device < 64) {
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 32; ++i) {
       if (done[device][i] == nullptr) {
         done[device][i] = (const void*)fn;
         break;
@@ -123,7 +108,7 @@ cudaError_t ensure_smem_attr(KernelFn fn, int device, size_t bytes) {
 size_t layout(fp8mm_plan_s* P, int stages) {
   const uint32_t x_bytes = kBlockM * kBlockK;
   const uint32_t y_bytes = (uint32_t)(P->bn / P->cg) * kBlockK;
-  const uint32_t sf_bytes = P->mx ? 512u * (1u + (uint32_t)(P->bn / 128)) : 0u;
+  const uint32_t sf_bytes = P->mx ? kSfStageBytes : 0u;
   uint32_t off = 0;
   P->x_stage_bytes = x_bytes;
   P->y_stage_bytes = y_bytes;
@@ -137,14 +122,25 @@ size_t layout(fp8mm_plan_s* P, int stages) {
   off += sf_bytes * stages;
   off = (off + 1023u) & ~1023u;
   P->off_out = off;
-  off += kEpiWarps * kStageOutBytes;
+  off += (uint32_t)(P->ew * stage_out_bytes(P->ew));
   P->off_ys = off;
-  if (P->x_kind != kScaleNone) off += kEpiWarps * (P->bn / 2) * 4;
+  if (P->x_kind != kScaleNone) off += (uint32_t)(P->ew * part_max_cols(P->bn, P->ew) * 4);
   off = (off + 127u) & ~127u;
   P->off_bar = off;
-  off += 16u * stages + 48u + 16u;  // full/empty per stage, 2+2 accumulator barriers, epilogue, drain, misc
+  off += 16u * stages + 80u + 16u;  // full/empty per stage, 4+4 accumulator barriers, epilogue, drain, misc
   off = (off + 127u) & ~127u;
   return (size_t)off + 1024;  // slack for aligning the dynamic base to 1024
+}
+
+// Relative mainloop throughput of a single-CTA tile width (measured on
+// GB300 with long K: narrower tiles move more bytes per MMA cycle).
+double width_efficiency(int bn, bool mx) {
+  switch (bn) {
+    case 256: return mx ? 0.85 : 1.0;  // the MX form keeps one accumulator at 256 columns
+    case 224: return 0.97;
+    case 192: return 0.93;
+    default: return 0.6;
+  }
 }
 
 }  // namespace
@@ -176,25 +172,26 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   if (d.fast_accum < 0 || d.fast_accum > 1) return FP8MM_ERR_INVALID;
   if (d.splitk < 0 || d.swap_ab < 0 || d.swap_ab > 2 || d.device < 0) return FP8MM_ERR_INVALID;
   if (d.cta_pair < 0 || d.cta_pair > 2) return FP8MM_ERR_INVALID;
-  if (d.reserved[0] || d.reserved[1]) return FP8MM_ERR_INVALID;
-  if (d.block_n != 0 && d.block_n != 16 && d.block_n != 32 && d.block_n != 64 && d.block_n != 128 &&
-      d.block_n != 256)
-    return FP8MM_ERR_INVALID;
+  if (d.epi_warps != 0 && d.epi_warps != 8 && d.epi_warps != 16) return FP8MM_ERR_INVALID;
+  if (d.stages < 0 || d.stages == 1 || d.stages > 12) return FP8MM_ERR_INVALID;
+  if (d.block_n != 0 && !(d.block_n >= 16 && d.block_n <= 256 && d.block_n % 16 == 0)) return FP8MM_ERR_INVALID;
   const int64_t lim = (int64_t)1 << 31;
   if (d.M >= lim || d.N >= lim || d.K >= lim || d.L >= 65536) return FP8MM_ERR_UNSUPPORTED;
   if (d.K % 16 != 0) return FP8MM_ERR_ALIGNMENT;
   if ((d.N * out_size(d.out_dtype)) % 16 != 0) return FP8MM_ERR_ALIGNMENT;
   const bool mx = d.scale_mode == FP8MM_SCALE_MX32_UE8M0;
   if (mx && d.a_fmt != d.b_fmt) return FP8MM_ERR_UNSUPPORTED;
-  if (mx && d.block_n != 0 && d.block_n < 128) return FP8MM_ERR_UNSUPPORTED;
 
   fp8mm_plan_s* P = new (std::nothrow) fp8mm_plan_s();
   if (!P) return FP8MM_ERR_INVALID;
+  struct Guard {
+    fp8mm_plan_s*& p;
+    ~Guard() { delete p; }
+  } guard{P};
   P->d = d;
   if (cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess ||
       cudaDeviceGetAttribute(&P->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device) != cudaSuccess) {
     cudaGetLastError();
-    delete P;
     return FP8MM_ERR_CUDA;
   }
   P->mx = mx ? 1 : 0;
@@ -210,7 +207,6 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     swap = false;
   else
     swap = !mx && d.M <= 256 && d.N > d.M;
-  if (mx && swap && d.M < 128) swap = false;
   P->swap = swap ? 1 : 0;
   P->R = swap ? d.N : d.M;
   P->Q = swap ? d.M : d.N;
@@ -224,48 +220,60 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     }
   }
   P->num_kb = (int)cdiv(d.K, kBlockK);
-  const int64_t tiles_r = std::max<int64_t>(1, cdiv(P->R, kBlockM));
+  const int64_t L = std::max<int64_t>(1, d.L);
+  const int64_t tiles_r1 = std::max<int64_t>(1, cdiv(P->R, kBlockM));
 
-  // Tile width on the MMA's N side.
+  // Tile width on the MMA's N side.  Wide problems pick the width whose
+  // whole waves over the SMs cost least; narrow ones the smallest
+  // power-of-two width that covers Q.
   int bn = d.block_n;
   if (bn == 0) {
     const int64_t q16 = std::max<int64_t>(16, cdiv(P->Q, 16) * 16);
-    bn = 16;
-    while (bn < q16 && bn < 256) bn *= 2;
-    if (mx && bn < 128) bn = 128;
-    // Skinny (swapped) problems are bound by streaming X from HBM: split the
-    // Y side in two when that turns 1-2 waves of tiles into ~3.
-    if (swap && bn == 256 && tiles_r * 2 <= 3 * (int64_t)P->sms) bn = 128;
-    // Slow accumulation keeps BN/2 fp32 sums per epilogue thread in registers;
-    // the MX form double-buffers its TMEM accumulator next to the factor ring.
-    if ((P->slow || mx) && bn > 128) bn = 128;
-  } else if (P->slow && bn > 128) {
-    delete P;
-    return FP8MM_ERR_UNSUPPORTED;
-  }
-  P->bn = bn;
-  // Two-SM pair tiles (cta_group::2): each SM stages its 128 rows of X and
-  // half of the Y tile, so a K step moves a third fewer bytes per MMA cycle
-  // into shared memory than a single-CTA 128 x 256 tile.
-  {
-    const bool pair_ok = !mx && (P->slow ? bn == 128 : (bn == 256 || bn == 128));
-    if (d.cta_pair == 1) {
-      if (!pair_ok) {
-        delete P;
-        return FP8MM_ERR_UNSUPPORTED;
+    int pw = 16;
+    while (pw < q16 && pw < 256) pw *= 2;
+    if (mx && pw < 128) pw = 128;
+    bn = pw;
+    if (swap) {
+      // Skinny problems stream X from HBM: split the Y side in two when that
+      // turns 1-2 waves of tiles into ~3.
+      if (bn == 256 && tiles_r1 * 2 <= 3 * (int64_t)P->sms) bn = 128;
+    } else if (!P->slow && P->Q > 128) {
+      double best = 1e300;
+      for (int c : {256, 224, 192, 128}) {
+        if (mx && c != 256 && c != 128) continue;
+        const int64_t tiles = tiles_r1 * cdiv(P->Q, c) * L;
+        const double cost = (double)cdiv(tiles, P->sms) * c / width_efficiency(c, mx);
+        if (cost < best * 0.999) {
+          best = cost;
+          bn = c;
+        }
       }
-      P->cg = 2;
-    } else if (d.cta_pair == 0) {
-      // Slow accumulation stays on single-CTA tiles: its per-chunk hand-off
-      // would wait on both CTAs' epilogues.
-      P->cg = (pair_ok && !swap && !P->slow && P->R >= 256 && bn == 256) ? 2 : 1;
     }
+    // Slow accumulation keeps the promoted sums in registers: at most 128 columns.
+    if (P->slow && bn > 128) bn = 128;
   }
-  const int64_t tiles_r_cg = std::max<int64_t>(1, cdiv(P->R, (int64_t)kBlockM * P->cg));
+  // MX tiles must start on a 128-row factor atom: the block-scaled MMA reads
+  // its factors from a TMEM column aligned to the atom's four columns.
+  if (mx && bn != 128 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
+  P->bn = bn;
+
+  // Two-SM pair tiles (cta_group::2) on request; measured no faster than
+  // single-CTA 128 x 256 tiles on GB300, so not chosen by default.
+  if (d.cta_pair == 1) {
+    if (mx || swap) return FP8MM_ERR_UNSUPPORTED;
+    P->cg = 2;
+  }
+  // Epilogue warps: 16 for slow accumulation at 128 columns (more TMEM loads
+  // in flight during the per-chunk promotion), else 8.
+  P->ew = d.epi_warps ? d.epi_warps : ((P->slow && !mx && bn == 128 && P->cg == 1) ? 16 : 8);
+  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew);
+  if (!fn) return FP8MM_ERR_UNSUPPORTED;
+
+  const int64_t tiles_r = std::max<int64_t>(1, cdiv(P->R, (int64_t)kBlockM * P->cg));
   const int64_t tiles_q = std::max<int64_t>(1, cdiv(P->Q, bn));
-  P->tiles_r = (int)tiles_r_cg;
+  P->tiles_r = (int)tiles_r;
   P->tiles_q = (int)tiles_q;
-  const int64_t tiles = tiles_r_cg * tiles_q * std::max<int64_t>(1, d.L);  // pair tiles when cg == 2
+  const int64_t tiles = tiles_r * tiles_q * L;  // pair tiles when cg == 2
 
   // Split-K: contiguous 128-aligned K ranges.  Chosen to fill whole waves of
   // SMs when there are fewer than two waves of tiles and the partial tiles
@@ -274,16 +282,16 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   const int64_t slots = P->sms / P->cg;  // concurrent work units (CTAs or CTA pairs)
   if (S == 0) {
     S = 1;
-    if (tiles < 2 * (int64_t)slots && P->num_kb >= 8) {
+    if (tiles < 2 * slots && P->num_kb >= 8) {
       double best = (double)tiles / (double)(cdiv(tiles, slots) * slots);
-      for (int s = 2; s <= 8; ++s) {
-        if (P->num_kb / s < 4) break;
-        if (bn > 128 && s > 2) break;
-        const int64_t u = tiles * s;
+      for (int sk = 2; sk <= 8; ++sk) {
+        if (P->num_kb / sk < 4) break;
+        if (bn > 128 && sk > 2) break;
+        const int64_t u = tiles * sk;
         const double eff = (double)u / (double)(cdiv(u, slots) * slots);
         if (eff > best + 0.05) {
           best = eff;
-          S = s;
+          S = sk;
         }
       }
     }
@@ -295,30 +303,39 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   P->grid = (int)std::min<long long>(P->units * P->cg, P->sms / P->cg * P->cg);
   P->group = swap ? 1 : 8;
 
-  // TMEM: accumulators, then (MX) a ring of scale-factor slots of 16 columns.
-  // Pipeline depth: as many stages as fit in shared memory (at most 12).
+  // Pipeline depth: as many stages as fit in shared memory (at most 12).  The
+  // MX form also keeps a 16-column TMEM slot per stage for its factors, next
+  // to two accumulators when they fit in 512 columns (else one).
   int stages = 12;
   while (stages > 2 && layout(P, stages) > (size_t)P->max_smem) --stages;
+  if (d.stages > 0) {
+    if (d.stages > stages) return FP8MM_ERR_UNSUPPORTED;
+    stages = d.stages;
+  }
+  // Slow accumulation hands each 128-K chunk to the epilogue: with 128-column
+  // tiles four chunk buffers fill the 512 TMEM columns and let the MMA run up
+  // to three chunks ahead of the promotion.
+  P->num_acc = (P->slow && !mx && 4 * bn <= 512) ? 4 : 2;
+  if (mx) {
+    const int tmem_stages = (512 - 2 * bn) / 16;
+    if (tmem_stages >= 3)
+      stages = std::min(stages, tmem_stages);
+    else
+      P->num_acc = 1;
+  } else if (2 * bn > 512) {
+    P->num_acc = 1;
+  }
   P->stages = stages;
   P->smem_bytes = layout(P, stages);
-  if (P->smem_bytes > (size_t)P->max_smem) {
-    delete P;
-    return FP8MM_ERR_UNSUPPORTED;
-  }
-  const uint32_t sf_cols = mx ? 16u * (uint32_t)stages : 0u;
-  P->num_acc = (2u * bn + sf_cols <= 512u) ? 2 : 1;
-  const uint32_t need = (uint32_t)(P->num_acc * bn) + sf_cols;
+  if (P->smem_bytes > (size_t)P->max_smem) return FP8MM_ERR_UNSUPPORTED;
+  const uint32_t need = (uint32_t)(P->num_acc * bn) + (mx ? 16u * (uint32_t)stages : 0u);
   uint32_t cols = 32;
   while (cols < need) cols *= 2;
-  if (cols > 512) {
-    delete P;
-    return FP8MM_ERR_UNSUPPORTED;
-  }
+  if (cols > 512) return FP8MM_ERR_UNSUPPORTED;
   P->tmem_cols = cols;
 
   if (P->cg == 2) {
     // Persistent grid: as many CTA pairs as can be resident at once.
-    KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg);
     int nclusters = 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -327,14 +344,13 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)P->grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kernel_threads(P->ew));
     cfg.dynamicSmemBytes = P->smem_bytes;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!fn || ensure_smem_attr(fn, d.device, (size_t)P->max_smem) != cudaSuccess ||
+    if (ensure_smem_attr(fn, d.device, (size_t)P->max_smem) != cudaSuccess ||
         cudaOccupancyMaxActiveClusters(&nclusters, (const void*)fn, &cfg) != cudaSuccess || nclusters < 1) {
       cudaGetLastError();
-      delete P;
       return FP8MM_ERR_CUDA;
     }
     P->grid = 2 * (int)std::min<long long>(P->units, nclusters);
@@ -346,6 +362,7 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     P->ws_bytes = P->ws_counters_off + ((P->ws_counters_bytes + 255) & ~(size_t)255);
   }
   *out = P;
+  P = nullptr;  // ownership passes to the caller
   return FP8MM_OK;
 }
 
@@ -386,6 +403,7 @@ fp8mm_status fp8mm_plan_get_info(const fp8mm_plan_t* plan, fp8mm_plan_info* info
   info->slow = plan->slow;
   info->smem_bytes = (int32_t)plan->smem_bytes;
   info->cta_pair = plan->cg == 2 ? 1 : 0;
+  info->epi_warps = plan->ew;
   return FP8MM_OK;
 }
 
@@ -406,11 +424,11 @@ fp8mm_status fp8mm_device_error(int device, uint32_t* code, int clear) {
   fp8mm_status st = FP8MM_OK;
   unsigned v = 0;
   if (cudaDeviceSynchronize() != cudaSuccess ||
-      cudaMemcpyFromSymbol(&v, g_fp8mm_abort, sizeof(v)) != cudaSuccess)
+      cudaMemcpyFromSymbol(&v, g_fp8mm_abort_word, sizeof(v)) != cudaSuccess)
     st = FP8MM_ERR_CUDA;
   if (st == FP8MM_OK && clear) {
     const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_fp8mm_abort, &zero, sizeof(zero)) != cudaSuccess) st = FP8MM_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_fp8mm_abort_word, &zero, sizeof(zero)) != cudaSuccess) st = FP8MM_ERR_CUDA;
   }
   *code = v;
   if (prev != device) cudaSetDevice(prev);
@@ -484,7 +502,7 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   }
   // One TMA store per warp covers 32 tile rows x `cw` tile columns, staged in
   // shared memory with the swizzle that matches its row length.
-  const int cw = chunk_cols(P->bn, P->out_es);
+  const int cw = chunk_cols(P->bn, P->out_es, P->ew);
   uint32_t rowbytes;
   cuuint32_t cbox[3];
   if (!P->swap) {
@@ -563,8 +581,9 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   kp.scale_kb = P->num_kb;
   kp.sfx_mb = (int)cdiv(P->R, 128);
   kp.sfy_mb = (int)cdiv(P->Q, 128);
-  kp.sfy_atoms = P->bn / 128 > 0 ? P->bn / 128 : 1;
   kp.amax_bits = reinterpret_cast<unsigned*>(amax);
+  kp.abort_word = abort_word_address(d.device);
+  if (!kp.abort_word) return FP8MM_ERR_CUDA;
   if (P->splits > 1) {
     kp.ws_partials = static_cast<float*>(workspace);
     kp.ws_counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + P->ws_counters_off);
@@ -582,7 +601,7 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   kp.out_swz_mask = swz_mask;
   kp.out_rowbytes = rowbytes;
 
-  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg);
+  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
   if (ensure_smem_attr(fn, d.device, (size_t)P->max_smem) != cudaSuccess) return FP8MM_ERR_CUDA;
   void* args[4] = {&tm_x, &tm_y, &tm_c, &kp};
@@ -593,7 +612,7 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)P->grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kernel_threads(P->ew));
   cfg.dynamicSmemBytes = P->smem_bytes;
   cfg.stream = stream;
   cfg.attrs = attr;

@@ -14,15 +14,15 @@
 // for skinny M the roles swap (X = B, Y = A) and the epilogue stores the
 // tile transposed, so that the long dimension fills the 128-row side.
 //
-// Roles (320 threads, one CTA per SM, persistent over work units):
-//   warps 0-7  epilogue: TMEM -> registers; for slow accumulation and block
-//              scales, one promotion per 128-K chunk (acc += s_x s_y chunk in
-//              fp32); split-K fix-up; scale, cast, NaN canonicalisation, amax,
-//              shared-memory staging and TMA stores.
-//   warp 8     TMA producer: A/B tiles (128 B of K per row, 128-byte swizzle)
+// Roles ((EW + 2) warps, one CTA per SM, persistent over work units):
+//   warps 0..EW-1  epilogue (EW = 8 or 16): TMEM -> registers; for slow
+//              accumulation and block scales, one promotion per 128-K chunk
+//              (acc += s_x s_y chunk in fp32); split-K fix-up; scale, cast,
+//              NaN canonicalisation, amax, shared-memory staging, TMA stores.
+//   warp EW    TMA producer: A/B tiles (128 B of K per row, 128-byte swizzle)
 //              and, for the MX form, the 512-byte scale-factor atoms, into a
 //              ring of `stages` shared-memory slots guarded by mbarriers.
-//   warp 9     MMA issuer: tcgen05.mma kind::f8f6f4 (or kind::mxf8f6f4 with
+//   warp EW+1  MMA issuer: tcgen05.mma kind::f8f6f4 (or kind::mxf8f6f4 with
 //              block scaling) into one or two TMEM accumulators; also owns
 //              the TMEM allocation.
 //
@@ -43,12 +43,24 @@ namespace fp8mm {
 constexpr int kBlockM = 128;      // MMA M: TMEM lanes per tile
 constexpr int kBlockK = 128;      // K per pipeline stage: one 128-byte swizzle row per operand row
 constexpr int kUmmaK = 32;        // K per tcgen05.mma for 8-bit operands
-constexpr int kEpiWarps = 8;
-constexpr int kProdWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
-constexpr int kStageOutBytes = 4096;  // per-warp output staging: two 2 KiB buffers
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+// Block geometry shared by the kernel and the host planner.
+__host__ __device__ constexpr int kernel_threads(int ew) { return (ew + 2) * 32; }
+// Per-warp output staging: two buffers of 32 rows x 64 B (8 epilogue warps)
+// or 32 rows x 32 B (16 epilogue warps).
+__host__ __device__ constexpr int stage_out_bytes(int ew) { return ew == 8 ? 4096 : 2048; }
+// Columns [0, half0_cols) belong to epilogue warps 0-3, the rest to warps 4-7.
+__host__ __device__ constexpr int half0_cols(int bn) { return bn <= 64 ? bn / 2 : ((bn / 2 + 31) / 32) * 32; }
+// Widest column range of one epilogue warp.
+__host__ __device__ constexpr int part_max_cols(int bn, int ew) { return ew == 8 ? half0_cols(bn) : bn / 4; }
+// Columns of one output chunk (one TMA store of 32 tile rows).
+__host__ __device__ constexpr int chunk_cols(int bn, int es, int ew) {
+  return ((ew == 8 ? 64 : 32) / es) < part_max_cols(bn, ew) ? ((ew == 8 ? 64 : 32) / es) : part_max_cols(bn, ew);
+}
+// MX: shared-memory bytes per stage for the factor atoms (X's atom and up to
+// three of Y's when the tile is not aligned to 128 rows).
+constexpr uint32_t kSfStageBytes = 2048;
 
 // Abort codes (OR-ed into the device word).
 constexpr unsigned kErrProducer = 1u, kErrMmaFull = 2u, kErrMmaAcc = 4u, kErrEpiAcc = 8u,
@@ -68,7 +80,7 @@ struct KParams {
   int out_dtype;          // 0 f32, 1 bf16, 2 f16
   int out_es;             // bytes per output element
   int stages;
-  int num_acc;            // TMEM accumulators (1 or 2)
+  int num_acc;            // TMEM accumulators (1, 2 or 4)
   uint32_t tmem_cols;
   uint32_t idesc;         // instruction descriptor without the scale-factor ids
   const float* sa_tensor; // per-tensor scales (device), or null
@@ -81,18 +93,16 @@ struct KParams {
   const uint8_t* sfx;     // MX scale-factor atoms of X and Y
   const uint8_t* sfy;
   int sfx_mb, sfy_mb;     // ceil(R / 128), ceil(Q / 128)
-  int sfy_atoms;          // atoms of Y per stage (BN / 128)
   float* ws_partials;     // split-K partial tiles [tile][split][col][row]
   unsigned* ws_counters;  // split-K arrivals per tile
   unsigned* amax_bits;    // fp32 amax as its bit pattern (non-negative floats order as uints)
+  unsigned* abort_word;   // device word recording aborted waits (read by fp8mm_device_error)
   uint32_t off_x, off_y, off_sf, off_out, off_ys, off_bar;  // shared-memory layout
   uint32_t x_stage_bytes, y_stage_bytes, sf_stage_bytes;
   uint32_t out_swz_mask;  // 16-byte-chunk XOR mask of the output staging swizzle
   uint32_t out_rowbytes;  // bytes per staging row
 };
 
-// Device word recording aborted waits (read by fp8mm_device_error).
-__device__ unsigned g_fp8mm_abort = 0u;
 
 struct Unit {
   int l, tr, tq, s, kb0, kb1;
@@ -120,7 +130,7 @@ __device__ __forceinline__ Unit decode_unit(long long u, const KParams& p) {
 // Bounded wait on an mbarrier phase.  Returns false if another role aborted or
 // the limit was hit (which sets the abort flag and the device error word).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                         unsigned code) {
+                                         unsigned* abort_word, unsigned code) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   uint32_t spins = 0;
@@ -130,7 +140,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       if (*abort_flag) return false;
       if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1u;
-        atomicOr(&g_fp8mm_abort, code);
+        atomicOr(abort_word, code);
         return false;
       }
     }
@@ -138,11 +148,11 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // Bounded wait used while tearing down: ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned* abort_word) {
   const uint64_t t0 = ptx::globaltimer_ns();
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(&g_fp8mm_abort, kErrDrain);
+      atomicOr(abort_word, kErrDrain);
       return;
     }
   }
@@ -167,13 +177,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t off, uint32_t mask) {
   return off ^ (((off >> 7) & mask) << 4);
 }
 
-// Columns of one output chunk: staging rows of 64 bytes (32 bf16/fp16 or 16
-// fp32 values), or the whole column range of a warp when that is narrower.
-__host__ __device__ constexpr int chunk_cols(int bn, int es) {
-  return (es == 4) ? (bn >= 32 ? 16 : bn / 2) : (bn >= 64 ? 32 : bn / 2);
-}
-// Columns [0, half0_cols) belong to epilogue warps 0-3, the rest to warps 4-7.
-__host__ __device__ constexpr int half0_cols(int bn) { return bn <= 64 ? bn / 2 : ((bn / 2 + 31) / 32) * 32; }
 
 // Packed fp32 pairs (Blackwell f32x2 arithmetic).
 __device__ __forceinline__ void mul2(float& x0, float& x1, float a0, float a1) {
@@ -299,25 +302,28 @@ __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap*
   }
 }
 
-// Epilogue warps 0-7.  Warp w reads TMEM lanes 32*(w%4) .. +31 (the tile rows
-// it may access) and the columns of half w/4.  Per work unit: (slow) promote
+// Epilogue warps 0..EW-1.  Warp w reads TMEM lanes 32*(w%4) .. +31 (the tile
+// rows it may access) and the columns of part w/4 (two parts for 8 warps,
+// four for 16).  Per work unit: (slow) promote
 // each 128-K chunk into fp32 registers; (split-K) publish the partial tile and
 // let the last arrival finish it; then scale, cast, amax and store.
-template <int BN, bool SLOW, int CG, int CW, int ES>
+template <int BN, bool SLOW, int CG, int EW, int CW, int ES>
 __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm_c, uint8_t* sgen, uint32_t sbase,
                                          uint32_t tmem_base, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t bar_epi,
                                          volatile uint32_t* misc, volatile uint32_t* abort_flag, uint32_t rank,
                                          long long u_first, long long u_step, int warp, int lane) {
-  constexpr int H0 = half0_cols(BN);
-  constexpr int HMAX = H0;                    // widest column range of a warp
+  constexpr int HMAX = part_max_cols(BN, EW);  // widest column range of a warp
   constexpr int LDW = HMAX < 32 ? HMAX : 32;  // columns per tcgen05.ld while promoting
-  static_assert(!SLOW || H0 * 2 == BN, "slow accumulation splits the tile evenly");
-  static_assert(H0 % CW == 0 && (BN - H0) % CW == 0, "chunks tile each half");
+  static_assert(EW == 8 || EW == 16, "8 or 16 epilogue warps");
+  static_assert(EW == 8 || BN % 128 == 0, "16 epilogue warps split 128-multiple tiles in four");
+  static_assert(!SLOW || HMAX * (EW / 4) == BN, "slow accumulation splits the tile evenly");
+  static_assert(HMAX % CW == 0 && (BN - HMAX) % CW == 0, "chunks tile each part");
+  constexpr int kStageOut = stage_out_bytes(EW);
   const int qd = warp & 3;
   const int h = warp >> 2;
   const int row = qd * 32 + lane;
-  const int col0 = h ? H0 : 0;
-  const int ncols = h ? BN - H0 : H0;
+  const int col0 = (EW == 8) ? (h ? HMAX : 0) : h * HMAX;
+  const int ncols = (EW == 8) ? (h ? BN - HMAX : HMAX) : HMAX;
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
   uint32_t abuf = 0, aphase = 0, epi_phase = 0;
   float amax_f = 0.0f;
@@ -325,8 +331,8 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   bool ok = true;
   const float alpha = p.sa_tensor ? (__ldg(p.sa_tensor) * __ldg(p.sb_tensor)) : 1.0f;
   float* ys_w = reinterpret_cast<float*>(sgen + p.off_ys) + warp * HMAX;
-  uint8_t* stg = sgen + p.off_out + warp * kStageOutBytes;
-  const uint32_t stg_s = sbase + p.off_out + warp * kStageOutBytes;
+  uint8_t* stg = sgen + p.off_out + warp * kStageOut;
+  const uint32_t stg_s = sbase + p.off_out + warp * kStageOut;
   uint32_t stg_sel = 0;
   float acc[SLOW ? HMAX : 1];  // slow accumulation: fp32 running sum of the promoted chunks
   (void)acc;
@@ -342,10 +348,8 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
       else
         ptx::mbar_arrive(bar_tempty + 8u * abuf);
     }
-    if (p.num_acc == 2) {
-      abuf ^= 1u;
-      if (abuf == 0) aphase ^= 1u;
-    } else {
+    if (++abuf == (uint32_t)p.num_acc) {
+      abuf = 0;
       aphase ^= 1u;
     }
   };
@@ -380,7 +384,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
             __syncwarp();
           }
         }
-        if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, kErrEpiAcc)) {
+        if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, p.abort_word, kErrEpiAcc)) {
           ok = false;
           break;
         }
@@ -417,7 +421,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
       }
       if (!ok) break;
     } else {
-      if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, kErrEpiAcc)) {
+      if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, p.abort_word, kErrEpiAcc)) {
         ok = false;
         break;
       }
@@ -458,7 +462,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
       __threadfence();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_epi);
-      if (!wait_bar(bar_epi, epi_phase, abort_flag, kErrEpiSync)) {
+      if (!wait_bar(bar_epi, epi_phase, abort_flag, p.abort_word, kErrEpiSync)) {
         ok = false;
         break;
       }
@@ -469,7 +473,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_epi);
-      if (!wait_bar(bar_epi, epi_phase, abort_flag, kErrEpiSync)) {
+      if (!wait_bar(bar_epi, epi_phase, abort_flag, p.abort_word, kErrEpiSync)) {
         ok = false;
         break;
       }
@@ -498,8 +502,8 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
             }
           }
           const int q0 = t.tq * BN + col0 + ci * CW;  // Y row of the chunk's first column
-          store_chunk<CW, ES>(p, tm_c, v, alpha, row_ok, q0, lane, stg + stg_sel * (kStageOutBytes / 2),
-                              stg_s + stg_sel * (kStageOutBytes / 2), p.swap ? r0 : q0, p.swap ? q0 : r0, t.l,
+          store_chunk<CW, ES>(p, tm_c, v, alpha, row_ok, q0, lane, stg + stg_sel * (kStageOut / 2),
+                              stg_s + stg_sel * (kStageOut / 2), p.swap ? r0 : q0, p.swap ? q0 : r0, t.l,
                               q0 < p.Q && r0 < p.R, amax_f, amax_nan);
           stg_sel ^= 1u;
         }
@@ -514,13 +518,13 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   if (lane == 0 && amax_local != 0u) atomicMax(p.amax_bits, amax_local);
 }
 
-template <int BN, bool SLOW, bool MX, int CG>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, bool SLOW, bool MX, int CG, int EW>
+__global__ void __launch_bounds__(kernel_threads(EW), 1)
     fp8mm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                  const __grid_constant__ CUtensorMap tm_c, const KParams p) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
-  static_assert(!MX || BN >= 128, "MX tiles cover whole 128-row scale-factor atoms");
-  static_assert(!SLOW || BN <= 128, "slow accumulation keeps BN/2 fp32 sums per thread in registers");
+  static_assert(!MX || BN == 128 || BN == 256, "MX tiles start on a 128-row factor atom");
+  static_assert(!SLOW || BN <= 128, "slow accumulation keeps its promoted sums in registers");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
   static_assert(!MX || CG == 1, "the block-scaled form runs on single-CTA tiles");
   extern __shared__ uint8_t smem_raw[];
@@ -528,6 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = (sraw + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - sraw);
 
+  constexpr int kProdWarp = EW;
+  constexpr int kMmaWarp = EW + 1;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
@@ -542,10 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_full = sbase + p.off_bar;
   const uint32_t bar_empty = bar_full + 8u * S;
   const uint32_t bar_tfull = bar_empty + 8u * S;
-  const uint32_t bar_tempty = bar_tfull + 16u;
-  const uint32_t bar_epi = bar_tempty + 16u;
+  const uint32_t bar_tempty = bar_tfull + 32u;  // up to four accumulators
+  const uint32_t bar_epi = bar_tempty + 32u;
   const uint32_t bar_done = bar_epi + 8u;
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sgen + p.off_bar + 16u * S + 48u);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sgen + p.off_bar + 16u * S + 80u);
   // misc[0] TMEM base address, misc[1] abort flag, misc[2] split-K ticket
 
   if (threadIdx.x == 0) {
@@ -553,11 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar_full + 8u * s, 1);
       ptx::mbar_init(bar_empty + 8u * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 4; ++b) {
       ptx::mbar_init(bar_tfull + 8u * b, 1);
-      ptx::mbar_init(bar_tempty + 8u * b, kEpiWarps * CG);  // the pair's epilogue warps arrive on the leader
+      ptx::mbar_init(bar_tempty + 8u * b, EW * CG);  // the pair's epilogue warps arrive on the leader
     }
-    ptx::mbar_init(bar_epi, kEpiWarps);
+    ptx::mbar_init(bar_epi, EW);
     ptx::mbar_init(bar_done, 1);
     misc[1] = 0u;
     misc[2] = 0u;
@@ -589,13 +595,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       // With a CTA pair both CTAs' copies complete on the leader's full barrier,
       // which the leader arms with the bytes of both.
-      const uint32_t tx = CG * (p.x_stage_bytes + p.y_stage_bytes) + (MX ? 512u * (1 + p.sfy_atoms) : 0u);
       for (long long u = u_first; ok && u < p.units; u += u_step) {
         const Unit t = decode_unit(u, p);
         const int xrow0 = t.tr * kBlockM * CG + (int)rank * kBlockM;
         const int yrow0 = t.tq * BN + (int)rank * (BN / CG);
+        // MX: Y's tile may start inside a 128-row atom; copy every atom it touches.
+        const int y_atom0 = (t.tq * BN) / 128;
+        const int y_atoms = MX ? ((t.tq * BN) % 128 + BN + 127) / 128 : 0;
+        const uint32_t tx = CG * (p.x_stage_bytes + p.y_stage_bytes) + (MX ? 512u * (1 + y_atoms) : 0u);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
-          if (!wait_bar(bar_empty + 8u * stage, phase ^ 1u, abort_flag, kErrProducer)) {
+          if (!wait_bar(bar_empty + 8u * stage, phase ^ 1u, abort_flag, p.abort_word, kErrProducer)) {
             ok = false;
             break;
           }
@@ -617,9 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint8_t* gx =
                 p.sfx + (((size_t)t.l * p.sfx_mb + t.tr) * p.scale_kb + kb) * 512u;
             ptx::bulk_load(sf, gx, 512u, fb);
-            for (int i = 0; i < p.sfy_atoms; ++i) {
+            for (int i = 0; i < y_atoms; ++i) {
               // atoms past the last row block are clamped to it; their rows are never stored
-              const int mb = min(t.tq * p.sfy_atoms + i, p.sfy_mb - 1);
+              const int mb = min(y_atom0 + i, p.sfy_mb - 1);
               const uint8_t* gy = p.sfy + (((size_t)t.l * p.sfy_mb + mb) * p.scale_kb + kb) * 512u;
               ptx::bulk_load(sf + 512u * (1 + i), gy, 512u, fb);
             }
@@ -638,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pair the leader's barriers also track the peer's copies.
       if (leader) {
         for (int s = 0; s < S; ++s) {
-          if (narm > s) drain_wait(bar_full + 8u * s, ((uint32_t)s < stage) ? phase : (phase ^ 1u));
+          if (narm > s) drain_wait(bar_full + 8u * s, ((uint32_t)s < stage) ? phase : (phase ^ 1u), p.abort_word);
         }
       }
     }
@@ -653,13 +662,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool gstart = SLOW || kb == t.kb0;
           const bool gend = SLOW || kb == t.kb1 - 1;
           if (gstart) {
-            if (!wait_bar(bar_tempty + 8u * abuf, aphase ^ 1u, abort_flag, kErrMmaAcc)) {
+            if (!wait_bar(bar_tempty + 8u * abuf, aphase ^ 1u, abort_flag, p.abort_word, kErrMmaAcc)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after_sync();
           }
-          if (!wait_bar(bar_full + 8u * stage, phase, abort_flag, kErrMmaFull)) {
+          if (!wait_bar(bar_full + 8u * stage, phase, abort_flag, p.abort_word, kErrMmaFull)) {
             ok = false;
             break;
           }
@@ -669,11 +678,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = ptx::desc_sw128_kmajor(sbase + p.off_y + stage * p.y_stage_bytes);
           if constexpr (MX) {
             const uint32_t sf_smem = sbase + p.off_sf + stage * p.sf_stage_bytes;
+            // TMEM slot of 16 columns per stage: X's atom in columns 0-3, Y's
+            // atoms from column 4.  Row r of an atom sits in lane r % 32 of
+            // column r / 32, so a Y tile starting at row o of its first atom
+            // reads its factors from column 4 + o / 32 on.
             const uint32_t sf_x = tmem_base + (uint32_t)(p.num_acc * BN) + stage * 16u;
-            const uint32_t sf_y = sf_x + 4u;
+            const int y_atoms = ((t.tq * BN) % 128 + BN + 127) / 128;
+            const uint32_t sf_y = sf_x + 4u + (uint32_t)(((t.tq * BN) % 128) / 32);
             ptx::tmem_cp_32x128b_warpx4(sf_x, ptx::desc_sf_atom(sf_smem));
-            for (int i = 0; i < p.sfy_atoms; ++i)
-              ptx::tmem_cp_32x128b_warpx4(sf_y + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * (1 + i)));
+            for (int i = 0; i < y_atoms; ++i)
+              ptx::tmem_cp_32x128b_warpx4(sf_x + 4u + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * (1 + i)));
 #pragma unroll
             for (int k = 0; k < kBlockK / kUmmaK; ++k) {
               // scale-factor ids pick byte k of each 32-bit TMEM word: the K block of 32
@@ -699,10 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tc_commit_pair(bar_tfull + 8u * abuf, (uint16_t)0x3);
             else
               ptx::tc_commit(bar_tfull + 8u * abuf);
-            if (p.num_acc == 2) {
-              abuf ^= 1u;
-              if (abuf == 0) aphase ^= 1u;
-            } else {
+            if (++abuf == (uint32_t)p.num_acc) {
+              abuf = 0;
               aphase ^= 1u;
             }
           }
@@ -717,16 +729,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit_pair(bar_done, (uint16_t)0x1);
       else
         ptx::tc_commit(bar_done);
-      drain_wait(bar_done, 0);
+      drain_wait(bar_done, 0, p.abort_word);
     }
-  } else {
+  } else if (warp < EW) {
     // ------------------------------------------------------------ epilogue
     if (p.out_es == 4)
-      epilogue<BN, SLOW, CG, chunk_cols(BN, 4), 4>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty, bar_epi,
-                                                    misc, abort_flag, rank, u_first, u_step, warp, lane);
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 4, EW), 4>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+                                                            bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
+                                                            lane);
     else
-      epilogue<BN, SLOW, CG, chunk_cols(BN, 2), 2>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty, bar_epi,
-                                                    misc, abort_flag, rank, u_first, u_step, warp, lane);
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 2, EW), 2>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+                                                            bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
+                                                            lane);
   }
 
   ptx::tc_fence_before_sync();
@@ -747,4 +761,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+}  // namespace fp8mm
+
+namespace fp8mm {
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const KParams);
 }  // namespace fp8mm

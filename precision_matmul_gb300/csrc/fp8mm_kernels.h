@@ -1,0 +1,67 @@
+// fp8mm_kernels.h -- the kernel instantiations this library ships and the
+// table that selects one by tile width, accumulation mode, scale form, CTA
+// pairing and epilogue warp count.
+#pragma once
+#include "fp8mm_kernel.cuh"
+
+namespace fp8mm {
+
+KernelFn kernel_bn16_fast_f8_cg1_ew8();
+KernelFn kernel_bn32_fast_f8_cg1_ew8();
+KernelFn kernel_bn64_fast_f8_cg1_ew8();
+KernelFn kernel_bn16_slow_f8_cg1_ew8();
+KernelFn kernel_bn32_slow_f8_cg1_ew8();
+KernelFn kernel_bn64_slow_f8_cg1_ew8();
+KernelFn kernel_bn128_fast_f8_cg1_ew8();
+KernelFn kernel_bn192_fast_f8_cg1_ew8();
+KernelFn kernel_bn224_fast_f8_cg1_ew8();
+KernelFn kernel_bn256_fast_f8_cg1_ew8();
+KernelFn kernel_bn256_fast_f8_cg2_ew8();
+KernelFn kernel_bn128_fast_f8_cg2_ew8();
+KernelFn kernel_bn128_slow_f8_cg2_ew8();
+KernelFn kernel_bn128_slow_f8_cg1_ew8();
+KernelFn kernel_bn128_slow_f8_cg1_ew16();
+KernelFn kernel_bn128_fast_mx_cg1_ew8();
+KernelFn kernel_bn256_fast_mx_cg1_ew8();
+KernelFn kernel_bn128_slow_mx_cg1_ew8();
+
+struct KernelEntry {
+  int bn, slow, mx, cg, ew;
+  KernelFn (*get)();
+};
+
+inline const KernelEntry* kernel_table(int* n) {
+  static const KernelEntry table[] = {
+      {16, 0, 0, 1, 8, &kernel_bn16_fast_f8_cg1_ew8},
+      {32, 0, 0, 1, 8, &kernel_bn32_fast_f8_cg1_ew8},
+      {64, 0, 0, 1, 8, &kernel_bn64_fast_f8_cg1_ew8},
+      {16, 1, 0, 1, 8, &kernel_bn16_slow_f8_cg1_ew8},
+      {32, 1, 0, 1, 8, &kernel_bn32_slow_f8_cg1_ew8},
+      {64, 1, 0, 1, 8, &kernel_bn64_slow_f8_cg1_ew8},
+      {128, 0, 0, 1, 8, &kernel_bn128_fast_f8_cg1_ew8},
+      {192, 0, 0, 1, 8, &kernel_bn192_fast_f8_cg1_ew8},
+      {224, 0, 0, 1, 8, &kernel_bn224_fast_f8_cg1_ew8},
+      {256, 0, 0, 1, 8, &kernel_bn256_fast_f8_cg1_ew8},
+      {256, 0, 0, 2, 8, &kernel_bn256_fast_f8_cg2_ew8},
+      {128, 0, 0, 2, 8, &kernel_bn128_fast_f8_cg2_ew8},
+      {128, 1, 0, 2, 8, &kernel_bn128_slow_f8_cg2_ew8},
+      {128, 1, 0, 1, 8, &kernel_bn128_slow_f8_cg1_ew8},
+      {128, 1, 0, 1, 16, &kernel_bn128_slow_f8_cg1_ew16},
+      {128, 0, 1, 1, 8, &kernel_bn128_fast_mx_cg1_ew8},
+      {256, 0, 1, 1, 8, &kernel_bn256_fast_mx_cg1_ew8},
+      {128, 1, 1, 1, 8, &kernel_bn128_slow_mx_cg1_ew8},
+  };
+  *n = (int)(sizeof(table) / sizeof(table[0]));
+  return table;
+}
+
+inline KernelFn select_kernel(int bn, bool slow, bool mx, int cg, int ew) {
+  int n = 0;
+  const KernelEntry* t = kernel_table(&n);
+  for (int i = 0; i < n; ++i)
+    if (t[i].bn == bn && t[i].slow == (int)slow && t[i].mx == (int)mx && t[i].cg == cg && t[i].ew == ew)
+      return t[i].get();
+  return nullptr;
+}
+
+}  // namespace fp8mm

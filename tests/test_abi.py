@@ -76,7 +76,8 @@ def _plan_status(**kw):
     (dict(M=16, N=16, K=16, out_dtype=3), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, scale_mode=4), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, fast_accum=2), B.FP8MM_ERR_INVALID),
-    (dict(M=16, N=16, K=16, block_n=48), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, block_n=40), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, epi_warps=12), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, swap_ab=3), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=24), B.FP8MM_ERR_ALIGNMENT),          # K rows not 16-byte multiples
     (dict(M=16, N=12, K=16), B.FP8MM_ERR_ALIGNMENT),          # bf16 C rows of 24 bytes
@@ -93,11 +94,11 @@ def test_plan_validation_before_cuda(lib, kw, status):
         assert st == status
 
 
-def test_reserved_fields_must_be_zero(lib):
-    d = B.make_desc(16, 16, 16)
-    d.reserved[1] = 7
-    h = ctypes.c_void_p()
-    assert B.load().fp8mm_plan(ctypes.byref(d), ctypes.byref(h)) == B.FP8MM_ERR_INVALID
+def test_stage_count_range(lib):
+    for bad in (1, 13, -1):
+        d = B.make_desc(16, 16, 16, stages=bad)
+        h = ctypes.c_void_p()
+        assert B.load().fp8mm_plan(ctypes.byref(d), ctypes.byref(h)) == B.FP8MM_ERR_INVALID
 
 
 def test_null_arguments(lib):

@@ -76,6 +76,14 @@ def test_mx_ragged():
     _run_check(p)
 
 
+@pytest.mark.parametrize("fmt", [synth.E4M3, synth.E5M2])
+def test_mx_wide_tiles(fmt):
+    # 256-column tiles: two factor atoms per stage, one TMEM accumulator
+    p = synth.mx_batched(L=2, M=264, N=520, K=384, fmt=fmt, seed=27)
+    c, amax, plan = _run_check(p, block_n=256)
+    assert plan.info()["block_n"] == 256
+
+
 @pytest.mark.parametrize("M", [16, 40, 64, 200])
 @pytest.mark.parametrize("data", ["gauss40", "adversarial"])
 @pytest.mark.parametrize("fast", [True, False])
