@@ -54,13 +54,17 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return obj
 
     workers = max(1, min(len(SOURCES), os.cpu_count() or 1))
-    with ThreadPoolExecutor(max_workers=workers) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.run([nvcc, ARCH, "-shared", *objs, "-o", tmp], check=True)
-    os.replace(tmp, LIB)
-    for o in objs:
-        os.remove(o)
+    objs = [os.path.join(BUILD, os.path.splitext(src)[0] + f".{os.getpid()}.o") for src in SOURCES]
+    try:
+        with ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(compile_one, SOURCES))
+        tmp = LIB + f".tmp{os.getpid()}"
+        subprocess.run([nvcc, ARCH, "-shared", *objs, "-o", tmp], check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB
 
 

@@ -237,7 +237,8 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
       // Skinny problems stream X from HBM: split the Y side in two when that
       // turns 1-2 waves of tiles into ~3.
       if (bn == 256 && tiles_r1 * 2 <= 3 * (int64_t)P->sms) bn = 128;
-    } else if (!P->slow && P->Q > 128) {
+    } else if (!P->slow && P->Q > 128 && tiles_r1 * cdiv(P->Q, 256) * L > (int64_t)P->sms) {
+      // (under one wave of 256-wide tiles the widest tile is the fastest)
       double best = 1e300;
       for (int c : {256, 224, 192, 128}) {
         if (mx && c != 256 && c != 128) continue;

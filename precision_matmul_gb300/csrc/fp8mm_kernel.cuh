@@ -43,7 +43,8 @@ namespace fp8mm {
 constexpr int kBlockM = 128;      // MMA M: TMEM lanes per tile
 constexpr int kBlockK = 128;      // K per pipeline stage: one 128-byte swizzle row per operand row
 constexpr int kUmmaK = 32;        // K per tcgen05.mma for 8-bit operands
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+// Bound on one wait: 2^31 SM clock cycles, about one second at GB300 clocks.
+constexpr uint64_t kWaitLimitCycles = 1ull << 31;
 
 // Block geometry shared by the kernel and the host planner.
 __host__ __device__ constexpr int kernel_threads(int ew) { return (ew + 2) * 32; }
@@ -132,13 +133,13 @@ __device__ __forceinline__ Unit decode_unit(long long u, const KParams& p) {
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                          unsigned* abort_word, unsigned code) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
+  const uint64_t t0 = ptx::clock_cycles();
   uint32_t spins = 0;
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((++spins & 15u) == 0) {
       if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (ptx::clock_cycles() - t0 > kWaitLimitCycles) {
         *abort_flag = 1u;
         atomicOr(abort_word, code);
         return false;
@@ -149,9 +150,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 // Bounded wait used while tearing down: ignores the abort flag.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned* abort_word) {
-  const uint64_t t0 = ptx::globaltimer_ns();
+  const uint64_t t0 = ptx::clock_cycles();
   while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (ptx::clock_cycles() - t0 > kWaitLimitCycles) {
       atomicOr(abort_word, kErrDrain);
       return;
     }
@@ -429,10 +430,22 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
     }
     // Fast accumulation reads the finished tile from TMEM chunk by chunk.
     const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
-    auto get_chunk = [&](int ci, float(&v)[CW]) {
+    // Slow accumulation: the chunk being stored is always acc[0 .. CW); after
+    // each chunk the sums rotate left by CW, so one copy of the loop body
+    // serves every chunk and a full pass restores the original order.
+    auto rotate_acc = [&](const float(&v)[CW]) {  // v: the chunk just read from acc[0 .. CW)
       if constexpr (SLOW) {
 #pragma unroll
-        for (int i = 0; i < CW; ++i) v[i] = acc[ci * CW + i];
+        for (int i = 0; i < HMAX - CW; ++i) acc[i] = acc[i + CW];
+#pragma unroll
+        for (int i = 0; i < CW; ++i) acc[HMAX - CW + i] = v[i];
+      }
+    };
+    auto get_chunk = [&](int ci, float(&v)[CW]) {
+      if constexpr (SLOW) {
+        (void)ci;
+#pragma unroll
+        for (int i = 0; i < CW; ++i) v[i] = acc[i];
       } else {
         uint32_t r[CW];
         tmem_load<CW>(taddr + ci * CW, r);
@@ -440,7 +453,6 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
         for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
       }
     };
-    constexpr int NCH_MAX = HMAX / CW;
     const int nch = ncols / CW;
 
     // ---------------------------------------------------- split-K fix-up
@@ -450,14 +462,15 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
       const long long tile = (((long long)t.l * p.tiles_r + t.tr) * p.tiles_q + t.tq) * CG + rank;
       tile_ws = p.ws_partials + (size_t)tile * p.splits * (kBlockM * BN);
       float* slot = tile_ws + (size_t)t.s * (kBlockM * BN);
+      // One copy of each loop body: a compact epilogue runs from the
+      // instruction cache from the first tile on.
+#pragma unroll 1
+      for (int ci = 0; ci < nch; ++ci) {
+        float v[CW];
+        get_chunk(ci, v);
+        rotate_acc(v);
 #pragma unroll
-      for (int ci = 0; ci < NCH_MAX; ++ci) {
-        if (ci < nch) {
-          float v[CW];
-          get_chunk(ci, v);
-#pragma unroll
-          for (int i = 0; i < CW; ++i) __stcg(slot + (size_t)(col0 + ci * CW + i) * kBlockM + row, v[i]);
-        }
+        for (int i = 0; i < CW; ++i) __stcg(slot + (size_t)(col0 + ci * CW + i) * kBlockM + row, v[i]);
       }
       __threadfence();
       __syncwarp();
@@ -485,11 +498,11 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
     // ---------------------------------------------------- scale, cast, store
     if (finish) {
       const int r0 = xbase + qd * 32;  // X row of the warp's first lane
-#pragma unroll
-      for (int ci = 0; ci < NCH_MAX; ++ci) {
-        if (ci < nch) {
+      auto finish_chunk = [&](int ci) {
+        {
           float v[CW];
           get_chunk(ci, v);
+          rotate_acc(v);
           if (p.splits > 1) {
             // Partials are added in split order 0..S-1 whichever CTA arrived last.
 #pragma unroll
@@ -507,7 +520,9 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
                               q0 < p.Q && r0 < p.R, amax_f, amax_nan);
           stg_sel ^= 1u;
         }
-      }
+      };
+#pragma unroll 1
+      for (int ci = 0; ci < nch; ++ci) finish_chunk(ci);
     }
     if constexpr (!SLOW) release_acc();
   }
@@ -590,6 +605,9 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      ptx::prefetch_tensormap(&tm_x);
+      ptx::prefetch_tensormap(&tm_y);
+      ptx::prefetch_tensormap(&tm_c);
       uint32_t stage = 0, phase = 0;
       long long narm = 0;
       bool ok = true;
