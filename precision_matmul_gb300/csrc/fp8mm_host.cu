@@ -234,9 +234,8 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     if (mx && pw < 128) pw = 128;
     bn = pw;
     if (swap) {
-      // Skinny problems stream X from HBM: split the Y side in two when that
-      // turns 1-2 waves of tiles into ~3.
-      if (bn == 256 && tiles_r1 * 2 <= 3 * (int64_t)P->sms) bn = 128;
+      // Skinny problems stream X (the long operand) from HBM once; the whole
+      // of Y fits one tile and split-K fills the waves.
     } else if (!P->slow && P->Q > 128 && tiles_r1 * cdiv(P->Q, 256) * L > (int64_t)P->sms) {
       // (under one wave of 256-wide tiles the widest tile is the fastest)
       double best = 1e300;
@@ -307,7 +306,8 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   // Pipeline depth: as many stages as fit in shared memory (at most 12).  The
   // MX form also keeps a 16-column TMEM slot per stage for its factors, next
   // to two accumulators when they fit in 512 columns (else one).
-  int stages = 12;
+  // (Streaming skinny shapes measured best at 6-8 stages on GB300.)
+  int stages = swap ? 8 : 12;
   while (stages > 2 && layout(P, stages) > (size_t)P->max_smem) --stages;
   if (d.stages > 0) {
     if (d.stages > stages) return FP8MM_ERR_UNSUPPORTED;

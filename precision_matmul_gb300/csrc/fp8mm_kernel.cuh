@@ -504,15 +504,28 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
           get_chunk(ci, v);
           rotate_acc(v);
           if (p.splits > 1) {
-            // Partials are added in split order 0..S-1 whichever CTA arrived last.
+            // Partials are added in split order 0..S-1 whichever CTA arrived
+            // last.  Each split's chunk is loaded as one batch of independent
+            // loads before it is added, so the loads overlap.
+            const float* base = tile_ws + (size_t)(col0 + ci * CW) * kBlockM + row;
+            float sum[CW];
 #pragma unroll
-            for (int i = 0; i < CW; ++i) {
-              const size_t off = (size_t)(col0 + ci * CW + i) * kBlockM + row;
-              float sum = (t.s == 0) ? v[i] : __ldcg(tile_ws + off);
-              for (int ss = 1; ss < p.splits; ++ss)
-                sum += (ss == t.s) ? v[i] : __ldcg(tile_ws + (size_t)ss * (kBlockM * BN) + off);
-              v[i] = sum;
+            for (int i = 0; i < CW; ++i) sum[i] = (t.s == 0) ? v[i] : __ldcg(base + (size_t)i * kBlockM);
+            for (int ss = 1; ss < p.splits; ++ss) {
+              float part[CW];
+              if (ss == t.s) {
+#pragma unroll
+                for (int i = 0; i < CW; ++i) part[i] = v[i];
+              } else {
+                const float* src = base + (size_t)ss * (kBlockM * BN);
+#pragma unroll
+                for (int i = 0; i < CW; ++i) part[i] = __ldcg(src + (size_t)i * kBlockM);
+              }
+#pragma unroll
+              for (int i = 0; i < CW; ++i) sum[i] += part[i];
             }
+#pragma unroll
+            for (int i = 0; i < CW; ++i) v[i] = sum[i];
           }
           const int q0 = t.tq * BN + col0 + ci * CW;  // Y row of the chunk's first column
           store_chunk<CW, ES>(p, tm_c, v, alpha, row_ok, q0, lane, stg + stg_sel * (kStageOut / 2),
