@@ -179,25 +179,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t off, uint32_t mask) {
 }
 
 
-// Packed fp32 pairs (Blackwell f32x2 arithmetic).
-__device__ __forceinline__ void mul2(float& x0, float& x1, float a0, float a1) {
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(x0), "=f"(x1)
-      : "f"(x0), "f"(x1), "f"(a0), "f"(a1));
-}
-__device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(c0), "=f"(c1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-__device__ __forceinline__ void add2(float& c0, float& c1, float b0, float b1) {
-  asm("{\n\t.reg .b64 rb, rc, rd;\n\tmov.b64 rb, {%2, %3};\n\tmov.b64 rc, {%4, %5};\n\t"
-      "add.rn.f32x2 rd, rc, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(c0), "=f"(c1)
-      : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
 // max that returns NaN if either input is NaN
 __device__ __forceinline__ float max_nan(float a, float b) {
   float r;
@@ -227,7 +208,7 @@ __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap*
                                             int cx, int cy, int cl, bool in_bounds, float& amax_f,
                                             uint32_t& amax_nan) {
 #pragma unroll
-  for (int i = 0; i < CW; i += 2) mul2(v[i], v[i + 1], alpha, alpha);
+  for (int i = 0; i < CW; ++i) v[i] *= alpha;
   // largest |value| of the chunk inside C (NaN-propagating)
   float m = 0.0f;
   if (row_ok && q0 + CW <= p.Q) {
@@ -396,26 +377,17 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
         for (int pc = 0; pc < HMAX / LDW; ++pc) {
           uint32_t r[LDW];
           tmem_load<LDW>(taddr + pc * LDW, r);
+          // One fp32 instruction per element (the promotion is issue-bound).
 #pragma unroll
-          for (int i = 0; i < LDW; i += 2) {
+          for (int i = 0; i < LDW; ++i) {
             const int j = pc * LDW + i;
-            const float v0 = __uint_as_float(r[i]), v1 = __uint_as_float(r[i + 1]);
-            if (g == 0) {
-              acc[j] = v0;
-              acc[j + 1] = v1;
-              if (p.x_kind != kScaleNone) {
-                if (p.y_kind == kScaleBlock128)
-                  mul2(acc[j], acc[j + 1], f, f);
-                else
-                  mul2(acc[j], acc[j + 1], xs * ys_w[j], xs * ys_w[j + 1]);
-              }
-            } else if (p.x_kind == kScaleNone) {
-              add2(acc[j], acc[j + 1], v0, v1);
-            } else if (p.y_kind == kScaleBlock128) {
-              fma2(acc[j], acc[j + 1], f, f, v0, v1);
-            } else {
-              fma2(acc[j], acc[j + 1], xs * ys_w[j], xs * ys_w[j + 1], v0, v1);
-            }
+            const float v = __uint_as_float(r[i]);
+            if (p.x_kind == kScaleNone)
+              acc[j] = (g == 0) ? v : acc[j] + v;
+            else if (p.y_kind == kScaleBlock128)
+              acc[j] = (g == 0) ? f * v : fmaf(f, v, acc[j]);
+            else
+              acc[j] = (g == 0) ? (xs * ys_w[j]) * v : fmaf(xs * ys_w[j], v, acc[j]);
           }
         }
         release_acc();
