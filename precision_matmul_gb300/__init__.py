@@ -81,7 +81,8 @@ def plan_for(desc_key: tuple) -> Plan:
             p = Plan(make_desc(*desc_key[:4], a_fmt=desc_key[4], b_fmt=desc_key[5], scale_mode=desc_key[6],
                                out_dtype=desc_key[7], fast_accum=desc_key[8], splitk=desc_key[9],
                                swap_ab=desc_key[10], block_n=desc_key[11], device=desc_key[12],
-                               cta_pair=desc_key[13] if len(desc_key) > 13 else 0))
+                               cta_pair=desc_key[13] if len(desc_key) > 13 else 0,
+                               epi_warps=desc_key[14] if len(desc_key) > 14 else 0))
             _plans[desc_key] = p
         return p
 
@@ -100,7 +101,7 @@ def _workspace(device, stream_handle, nbytes):
 
 
 def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a_fmt=None, b_fmt=None,
-              scale_mode=None, out=None, amax=None, splitk=0, swap_ab=0, block_n=0, cta_pair=0):
+              scale_mode=None, out=None, amax=None, splitk=0, swap_ab=0, block_n=0, cta_pair=0, epi_warps=0):
     """C = (a * scale_a) @ (b * scale_b)^T and amax = max |C|, on a's CUDA device.
 
     a: [M, K] or [L, M, K]; b: [N, K] or [L, N, K]; both K-contiguous FP8
@@ -108,7 +109,9 @@ def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a
     Scales are device tensors: fp32 one-element (per-tensor), fp32 1x128 /
     128x128 block scales, or uint8 / float8_e8m0fnu MX factor atoms.
     Returns (C, amax) with C of out_dtype (default bfloat16) and amax a
-    one-element fp32 tensor.  Enqueued on the current stream; nothing is
+    one-element fp32 tensor.  splitk, swap_ab, block_n, cta_pair and
+    epi_warps override the planner's choices (0 leaves them to it; meanings as
+    in fp8mm_desc).  Enqueued on the current stream; nothing is
     synchronised.  One workspace per (device, stream) is reused, so calls on
     one stream must not overlap with calls of another thread on that stream.
     """
@@ -132,7 +135,8 @@ def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a
     mode = scale_mode if scale_mode is not None else _infer_scale_mode(scale_a, scale_b, L, M, N, K)
     device = a.device.index if a.device.index is not None else torch.cuda.current_device()
     fast = 1 if use_fast_accum else 0
-    key = (M, N, K, L, fa, fb, int(mode), oc, fast, int(splitk), int(swap_ab), int(block_n), device, int(cta_pair))
+    key = (M, N, K, L, fa, fb, int(mode), oc, fast, int(splitk), int(swap_ab), int(block_n), device, int(cta_pair),
+           int(epi_warps))
     plan = plan_for(key)
     shape = (L, M, N) if batched else (M, N)
     if out is None:

@@ -122,9 +122,10 @@ size_t layout(fp8mm_plan_s* P, int stages) {
   off += sf_bytes * stages;
   off = (off + 1023u) & ~1023u;
   P->off_out = off;
-  off += (uint32_t)(P->ew * stage_out_bytes(P->ew));
+  off += (uint32_t)(P->ew * stage_out_bytes(P->ew, wide_slow(P->bn, P->slow != 0)));
   P->off_ys = off;
-  if (P->x_kind != kScaleNone) off += (uint32_t)(P->ew * part_max_cols(P->bn, P->ew) * 4);
+  // per-column Y scales of the current chunk, one row per epilogue warp
+  if (P->x_kind != kScaleNone && P->y_kind == kScaleRow) off += (uint32_t)(P->ew * part_max_cols(P->bn, P->ew) * 4);
   off = (off + 127u) & ~127u;
   P->off_bar = off;
   off += 16u * stages + 80u + 16u;  // full/empty per stage, 4+4 accumulator barriers, epilogue, drain, misc
@@ -236,6 +237,10 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     if (swap) {
       // Skinny problems stream X (the long operand) from HBM once; the whole
       // of Y fits one tile and split-K fills the waves.
+    } else if (P->slow && P->Q > 128) {
+      // Slow accumulation: 256 columns (full-rate MMAs, never split) when
+      // they fill the SMs, else 128 (split-K can fill the waves).
+      bn = (!mx && d.splitk <= 1 && tiles_r1 * cdiv(P->Q, 256) * L >= (int64_t)P->sms) ? 256 : 128;
     } else if (!P->slow && P->Q > 128 && tiles_r1 * cdiv(P->Q, 256) * L > (int64_t)P->sms) {
       // (under one wave of 256-wide tiles the widest tile is the fastest)
       double best = 1e300;
@@ -249,9 +254,12 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
         }
       }
     }
-    // Slow accumulation keeps the promoted sums in registers: at most 128 columns.
-    if (P->slow && bn > 128) bn = 128;
+    // Slow accumulation keeps the promoted sums in registers: 256 columns
+    // only for the unswapped, unsplit single-CTA form.
+    if (P->slow && bn > 128 && (bn != 256 || swap || mx || d.cta_pair == 1 || d.splitk > 1)) bn = 128;
   }
+  if (P->slow && bn > 128 && (bn != 256 || swap || mx || d.cta_pair == 1 || d.splitk > 1))
+    return FP8MM_ERR_UNSUPPORTED;
   // MX tiles must start on a 128-row factor atom: the block-scaled MMA reads
   // its factors from a TMEM column aligned to the atom's four columns.
   if (mx && bn != 128 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
@@ -264,8 +272,11 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     P->cg = 2;
   }
   // Epilogue warps: 16 for slow accumulation at 128 columns (more TMEM loads
-  // in flight during the per-chunk promotion), else 8.
-  P->ew = d.epi_warps ? d.epi_warps : ((P->slow && !mx && bn == 128 && P->cg == 1) ? 16 : 8);
+  // in flight during the per-chunk promotion) and for slow 256-column tiles
+  // with per-column Y scales (their per-chunk scale work spread wider), else 8.
+  const bool wide = wide_slow(bn, P->slow != 0);
+  const bool wide_ycol = wide && blockwise && P->y_kind == kScaleRow;
+  P->ew = d.epi_warps ? d.epi_warps : ((P->slow && !mx && bn == 128 && P->cg == 1) || wide_ycol ? 16 : 8);
   KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
 
@@ -282,7 +293,7 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   const int64_t slots = P->sms / P->cg;  // concurrent work units (CTAs or CTA pairs)
   if (S == 0) {
     S = 1;
-    if (tiles < 2 * slots && P->num_kb >= 8) {
+    if (!wide && tiles < 2 * slots && P->num_kb >= 8) {
       double best = (double)tiles / (double)(cdiv(tiles, slots) * slots);
       for (int sk = 2; sk <= 8; ++sk) {
         if (P->num_kb / sk < 4) break;
@@ -312,6 +323,11 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   if (d.stages > 0) {
     if (d.stages > stages) return FP8MM_ERR_UNSUPPORTED;
     stages = d.stages;
+  } else if (wide) {
+    // Slow 256-column tiles keep a shallow ring: the shared memory left over
+    // becomes L1 for their scale loads and register spills, which measured
+    // faster on GB300 than a deeper ring (3 stages, 2 with per-column scales).
+    stages = std::min(stages, wide_ycol ? 2 : 3);
   }
   // Slow accumulation hands each 128-K chunk to the epilogue: with 128-column
   // tiles four chunk buffers fill the 512 TMEM columns and let the MMA run up
@@ -503,7 +519,7 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   }
   // One TMA store per warp covers 32 tile rows x `cw` tile columns, staged in
   // shared memory with the swizzle that matches its row length.
-  const int cw = chunk_cols(P->bn, P->out_es, P->ew);
+  const int cw = chunk_cols(P->bn, P->out_es, P->ew, wide_slow(P->bn, P->slow != 0));
   uint32_t rowbytes;
   cuuint32_t cbox[3];
   if (!P->swap) {

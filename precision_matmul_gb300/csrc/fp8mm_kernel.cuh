@@ -48,16 +48,24 @@ constexpr uint64_t kWaitLimitCycles = 1ull << 31;
 
 // Block geometry shared by the kernel and the host planner.
 __host__ __device__ constexpr int kernel_threads(int ew) { return (ew + 2) * 32; }
+// Slow accumulation on 256-column tiles: each epilogue warp keeps 128 (8
+// warps) or 64 (16 warps) promoted fp32 sums per row in registers, so its
+// output chunks are narrow (32 bytes of a row) and staged in half the
+// shared memory.
+__host__ __device__ constexpr bool wide_slow(int bn, bool slow) { return slow && bn > 128; }
 // Per-warp output staging: two buffers of 32 rows x 64 B (8 epilogue warps)
-// or 32 rows x 32 B (16 epilogue warps).
-__host__ __device__ constexpr int stage_out_bytes(int ew) { return ew == 8 ? 4096 : 2048; }
+// or 32 rows x 32 B (16 epilogue warps, or 256-column slow tiles).  (Rows of
+// 16 B measured far slower: the stores then write half sectors.)
+__host__ __device__ constexpr int stage_out_bytes(int ew, bool ws) { return (ew == 8 && !ws) ? 4096 : 2048; }
 // Columns [0, half0_cols) belong to epilogue warps 0-3, the rest to warps 4-7.
 __host__ __device__ constexpr int half0_cols(int bn) { return bn <= 64 ? bn / 2 : ((bn / 2 + 31) / 32) * 32; }
 // Widest column range of one epilogue warp.
 __host__ __device__ constexpr int part_max_cols(int bn, int ew) { return ew == 8 ? half0_cols(bn) : bn / 4; }
 // Columns of one output chunk (one TMA store of 32 tile rows).
-__host__ __device__ constexpr int chunk_cols(int bn, int es, int ew) {
-  return ((ew == 8 ? 64 : 32) / es) < part_max_cols(bn, ew) ? ((ew == 8 ? 64 : 32) / es) : part_max_cols(bn, ew);
+__host__ __device__ constexpr int chunk_cols(int bn, int es, int ew, bool ws) {
+  return ws ? 32 / es
+            : (((ew == 8 ? 64 : 32) / es) < part_max_cols(bn, ew) ? ((ew == 8 ? 64 : 32) / es)
+                                                                   : part_max_cols(bn, ew));
 }
 // MX: shared-memory bytes per stage for the factor atoms (X's atom and up to
 // three of Y's when the tile is not aligned to 128 rows).
@@ -65,7 +73,7 @@ constexpr uint32_t kSfStageBytes = 2048;
 
 // Abort codes (OR-ed into the device word).
 constexpr unsigned kErrProducer = 1u, kErrMmaFull = 2u, kErrMmaAcc = 4u, kErrEpiAcc = 8u,
-                   kErrEpiSync = 16u, kErrDrain = 32u;
+                   kErrEpiSync = 16u, kErrDrain = 32u, kErrPlan = 64u;
 
 enum ScaleKind : int { kScaleNone = 0, kScaleRow = 1, kScaleBlock128 = 2 };
 
@@ -202,8 +210,10 @@ __device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
 // is monotone, so the largest rounded value is the rounded largest value),
 // stages the warp's 32 x CW block in one of its two shared-memory buffers and
 // stores it with one TMA copy at (cx, cy, cl).
-template <int CW, int ES>
-__device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap* tm_c, float (&v)[CW], float alpha,
+// v holds at least CW values (the chunk is its first CW); NOSWAP drops the
+// transposed staging of swapped operands from the code.
+template <int CW, int ES, int NV, bool NOSWAP = false>
+__device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap* tm_c, float (&v)[NV], float alpha,
                                             bool row_ok, int q0, int lane, uint8_t* stg_gen, uint32_t stg_s,
                                             int cx, int cy, int cl, bool in_bounds, float& amax_f,
                                             uint32_t& amax_nan) {
@@ -229,13 +239,13 @@ __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap*
       w[i] = ((bits & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FFFFFFFu : bits;
     }
     if (!has_nan) amax_f = fmaxf(amax_f, m);
-    if (!p.swap) {
+    if (NOSWAP || !p.swap) {
 #pragma unroll
       for (int c = 0; c < CW / 4; ++c) {
         const uint32_t off = swz((uint32_t)lane * p.out_rowbytes + c * 16u, p.out_swz_mask);
         *reinterpret_cast<uint4*>(stg_gen + off) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       }
-    } else {
+    } else if constexpr (!NOSWAP) {
 #pragma unroll
       for (int i = 0; i < CW; ++i) {
         const uint32_t off = swz((uint32_t)i * p.out_rowbytes + lane * 4u, p.out_swz_mask);
@@ -259,13 +269,13 @@ __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap*
                           : __half2float(__ushort_as_half((unsigned short)(cvt_f16x2(m, 0.0f) & 0xFFFFu)));
       amax_f = fmaxf(amax_f, mr);
     }
-    if (!p.swap) {
+    if (NOSWAP || !p.swap) {
 #pragma unroll
       for (int c = 0; c < CW / 8; ++c) {
         const uint32_t off = swz((uint32_t)lane * p.out_rowbytes + c * 16u, p.out_swz_mask);
         *reinterpret_cast<uint4*>(stg_gen + off) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       }
-    } else {
+    } else if constexpr (!NOSWAP) {
 #pragma unroll
       for (int i = 0; i < CW; ++i) {
         const uint32_t off = swz((uint32_t)i * p.out_rowbytes + lane * 2u, p.out_swz_mask);
@@ -295,12 +305,15 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
                                          volatile uint32_t* misc, volatile uint32_t* abort_flag, uint32_t rank,
                                          long long u_first, long long u_step, int warp, int lane) {
   constexpr int HMAX = part_max_cols(BN, EW);  // widest column range of a warp
-  constexpr int LDW = HMAX < 32 ? HMAX : 32;  // columns per tcgen05.ld while promoting
+  constexpr bool WIDE = wide_slow(BN, SLOW);     // 128 promoted sums per thread
+  // columns per tcgen05.ld while promoting (16 beside 128 sums, within 168 registers)
+  constexpr int LDW = HMAX < 32 ? HMAX : (WIDE ? 16 : 32);
   static_assert(EW == 8 || EW == 16, "8 or 16 epilogue warps");
   static_assert(EW == 8 || BN % 128 == 0, "16 epilogue warps split 128-multiple tiles in four");
   static_assert(!SLOW || HMAX * (EW / 4) == BN, "slow accumulation splits the tile evenly");
+  static_assert(!WIDE || CG == 1, "256-column slow tiles run on one CTA");
   static_assert(HMAX % CW == 0 && (BN - HMAX) % CW == 0, "chunks tile each part");
-  constexpr int kStageOut = stage_out_bytes(EW);
+  constexpr int kStageOut = stage_out_bytes(EW, WIDE);
   const int qd = warp & 3;
   const int h = warp >> 2;
   const int row = qd * 32 + lane;
@@ -316,7 +329,18 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   uint8_t* stg = sgen + p.off_out + warp * kStageOut;
   const uint32_t stg_s = sbase + p.off_out + warp * kStageOut;
   uint32_t stg_sel = 0;
-  float acc[SLOW ? HMAX : 1];  // slow accumulation: fp32 running sum of the promoted chunks
+  // Slow accumulation: fp32 running sums of the promoted chunks -- in pairs
+  // for the packed (two-lane) fp32 instructions on 256-column tiles, single
+  // on the narrower ones (which measured faster with scalar code).
+  static_assert(HMAX % 2 == 0, "column ranges pair up");
+  float acc1[(SLOW && !WIDE) ? HMAX : 1];
+  float2 acc2[WIDE ? HMAX / 2 : 1];
+  auto acc = [&](int i) -> float& {
+    if constexpr (WIDE)
+      return (i & 1) ? acc2[i >> 1].y : acc2[i >> 1].x;
+    else
+      return acc1[i];
+  };
   (void)acc;
   (void)ys_w;
   // The pair leader's accumulator-empty barrier collects both CTAs' warps.
@@ -341,7 +365,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
     const int xbase = t.tr * kBlockM * CG + (int)rank * kBlockM;  // first X row of this CTA's half
     const int xr = xbase + row;                                   // row of X this thread owns
     const bool row_ok = xr < p.R;
-    if constexpr (SLOW) {
+    if constexpr (SLOW && !WIDE) {
       // One hand-off per 128-K chunk: acc += s_x(row, c) * s_y(col, c) * chunk.
       for (int g = 0; g < t.kb1 - t.kb0; ++g) {
         float xs = 1.0f, yb = 1.0f;
@@ -353,8 +377,8 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
                      : __ldg(p.x_scale + ((size_t)t.l * ((p.R + 127) / 128) + xr / 128) * p.scale_kb + c);
           }
           if (p.y_kind == kScaleBlock128) {
-            // BN divides 128 and tiles start at multiples of BN: one scale per tile and chunk
-            const int yq = t.tq * BN;
+            // a warp's columns lie in one 128-column block: one scale per warp and chunk
+            const int yq = t.tq * BN + col0;
             yb = (yq < p.Q) ? __ldg(p.y_scale + ((size_t)t.l * ((p.Q + 127) / 128) + yq / 128) * p.scale_kb + c)
                             : 0.0f;
           } else {
@@ -383,14 +407,107 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
             const int j = pc * LDW + i;
             const float v = __uint_as_float(r[i]);
             if (p.x_kind == kScaleNone)
-              acc[j] = (g == 0) ? v : acc[j] + v;
+              acc1[j] = (g == 0) ? v : acc1[j] + v;
             else if (p.y_kind == kScaleBlock128)
-              acc[j] = (g == 0) ? f * v : fmaf(f, v, acc[j]);
+              acc1[j] = (g == 0) ? f * v : fmaf(f, v, acc1[j]);
             else
-              acc[j] = (g == 0) ? (xs * ys_w[j]) * v : fmaf(xs * ys_w[j], v, acc[j]);
+              acc1[j] = (g == 0) ? (xs * ys_w[j]) * v : fmaf(xs * ys_w[j], v, acc1[j]);
           }
         }
         release_acc();
+      }
+      if (!ok) break;
+    } else if constexpr (WIDE) {
+      // One hand-off per 128-K chunk: acc += s_x(row, c) * s_y(col, c) * chunk.
+      // The sums start at -0, which leaves the first product (even a zero)
+      // unchanged, so every chunk takes the same single instruction per element.
+#pragma unroll
+      for (int j = 0; j < HMAX / 2; ++j) acc2[j] = make_float2(-0.0f, -0.0f);
+      // Block scales of chunk g + 1 are loaded while chunk g is promoted.
+      constexpr int YSR = (HMAX + 31) / 32;  // per-column Y scales held per lane
+      auto load_scales = [&](int g, float& xs, float& yb, float (&ysr)[YSR]) {
+        xs = 1.0f;
+        yb = 1.0f;
+        if (p.x_kind == kScaleNone) return;
+        const int c = t.kb0 + g;
+        if (row_ok) {
+          xs = (p.x_kind == kScaleRow)
+                   ? __ldg(p.x_scale + ((size_t)t.l * p.R + xr) * p.scale_kb + c)
+                   : __ldg(p.x_scale + ((size_t)t.l * ((p.R + 127) / 128) + xr / 128) * p.scale_kb + c);
+        }
+        if (p.y_kind == kScaleBlock128) {
+          // a warp's columns lie in one 128-column block: one scale per warp and chunk
+          const int yq = t.tq * BN + col0;
+          yb = (yq < p.Q) ? __ldg(p.y_scale + ((size_t)t.l * ((p.Q + 127) / 128) + yq / 128) * p.scale_kb + c)
+                          : 0.0f;
+        } else {
+#pragma unroll
+          for (int i = 0; i < YSR; ++i) {
+            const int j = lane + 32 * i;
+            const int yq = t.tq * BN + col0 + j;
+            ysr[i] = (j < ncols && yq < p.Q) ? __ldg(p.y_scale + ((size_t)t.l * p.Q + yq) * p.scale_kb + c) : 0.0f;
+          }
+        }
+      };
+      auto stage_ys = [&](const float (&ysr)[YSR]) {
+        if (p.x_kind == kScaleNone || p.y_kind == kScaleBlock128) return;
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < YSR; ++i)
+          if (lane + 32 * i < HMAX) ys_w[lane + 32 * i] = ysr[i];
+        __syncwarp();
+      };
+      float xs, yb, ysr[YSR];
+      load_scales(0, xs, yb, ysr);
+      stage_ys(ysr);
+      const int nchunks = t.kb1 - t.kb0;
+      for (int g = 0; g < nchunks; ++g) {
+        float xs_n = 1.0f, yb_n = 1.0f, ysr_n[YSR];
+        if (g + 1 < nchunks) load_scales(g + 1, xs_n, yb_n, ysr_n);
+        if (!wait_bar(bar_tfull + 8u * abuf, aphase, abort_flag, p.abort_word, kErrEpiAcc)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after_sync();
+        const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
+        // One packed fp32 instruction per two elements.  Per-tensor scales
+        // (f = 1: fma(1, v, acc) rounds v + acc once, like an add) and 128x128
+        // blocks of Y take one factor per warp; per-column Y scales one per
+        // column.  Each form is its own straight-line loop: the promotion runs
+        // once per chunk and must stay small in the instruction cache.
+        if (p.x_kind == kScaleNone || p.y_kind == kScaleBlock128) {
+          const float f = xs * yb;
+          const float2 f2 = make_float2(f, f);
+#pragma unroll
+          for (int pc = 0; pc < HMAX / LDW; ++pc) {
+            uint32_t r[LDW];
+            tmem_load<LDW>(taddr + pc * LDW, r);
+#pragma unroll
+            for (int i = 0; i < LDW; i += 2) {
+              const int j = (pc * LDW + i) / 2;
+              acc2[j] = __ffma2_rn(f2, make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), acc2[j]);
+            }
+          }
+        } else {
+          const float2 xs2 = make_float2(xs, xs);
+#pragma unroll
+          for (int pc = 0; pc < HMAX / LDW; ++pc) {
+            uint32_t r[LDW];
+            tmem_load<LDW>(taddr + pc * LDW, r);
+#pragma unroll
+            for (int i = 0; i < LDW; i += 2) {
+              const int j = (pc * LDW + i) / 2;
+              const float2 s2 = __fmul2_rn(xs2, reinterpret_cast<const float2*>(ys_w)[j]);
+              acc2[j] = __ffma2_rn(s2, make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), acc2[j]);
+            }
+          }
+        }
+        release_acc();
+        if (g + 1 < nchunks) {
+          xs = xs_n;
+          yb = yb_n;
+          stage_ys(ysr_n);
+        }
       }
       if (!ok) break;
     } else {
@@ -408,16 +525,16 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
     auto rotate_acc = [&](const float(&v)[CW]) {  // v: the chunk just read from acc[0 .. CW)
       if constexpr (SLOW) {
 #pragma unroll
-        for (int i = 0; i < HMAX - CW; ++i) acc[i] = acc[i + CW];
+        for (int i = 0; i < HMAX - CW; ++i) acc(i) = acc(i + CW);
 #pragma unroll
-        for (int i = 0; i < CW; ++i) acc[HMAX - CW + i] = v[i];
+        for (int i = 0; i < CW; ++i) acc(HMAX - CW + i) = v[i];
       }
     };
     auto get_chunk = [&](int ci, float(&v)[CW]) {
       if constexpr (SLOW) {
         (void)ci;
 #pragma unroll
-        for (int i = 0; i < CW; ++i) v[i] = acc[i];
+        for (int i = 0; i < CW; ++i) v[i] = acc(i);
       } else {
         uint32_t r[CW];
         tmem_load<CW>(taddr + ci * CW, r);
@@ -430,7 +547,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
     // ---------------------------------------------------- split-K fix-up
     bool finish = true;
     float* tile_ws = nullptr;
-    if (p.splits > 1) {
+    if (!WIDE && p.splits > 1) {  // (256-column slow tiles are never split)
       const long long tile = (((long long)t.l * p.tiles_r + t.tr) * p.tiles_q + t.tq) * CG + rank;
       tile_ws = p.ws_partials + (size_t)tile * p.splits * (kBlockM * BN);
       float* slot = tile_ws + (size_t)t.s * (kBlockM * BN);
@@ -471,7 +588,20 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
     if (finish) {
       const int r0 = xbase + qd * 32;  // X row of the warp's first lane
       auto finish_chunk = [&](int ci) {
-        {
+        if constexpr (WIDE) {
+          // The promoted sums are stored in place: the chunk is acc[0 .. CW),
+          // then the others move down by CW.
+          const int q0 = t.tq * BN + col0 + ci * CW;
+          float v[CW];
+#pragma unroll
+          for (int i = 0; i < CW; ++i) v[i] = acc(i);
+          store_chunk<CW, ES, CW, true>(p, tm_c, v, alpha, row_ok, q0, lane, stg + stg_sel * (kStageOut / 2),
+                                          stg_s + stg_sel * (kStageOut / 2), q0, r0, t.l, q0 < p.Q && r0 < p.R,
+                                          amax_f, amax_nan);
+          stg_sel ^= 1u;
+#pragma unroll
+          for (int i = 0; i < (HMAX - CW) / 2; ++i) acc2[i] = acc2[i + CW / 2];
+        } else {
           float v[CW];
           get_chunk(ci, v);
           rotate_acc(v);
@@ -524,7 +654,8 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
                  const __grid_constant__ CUtensorMap tm_c, const KParams p) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(!MX || BN == 128 || BN == 256, "MX tiles start on a 128-row factor atom");
-  static_assert(!SLOW || BN <= 128, "slow accumulation keeps its promoted sums in registers");
+  static_assert(!SLOW || BN <= 128 || (BN == 256 && CG == 1 && !MX),
+                "slow accumulation keeps its promoted sums in registers: 256-column tiles on one CTA");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
   static_assert(!MX || CG == 1, "the block-scaled form runs on single-CTA tiles");
   extern __shared__ uint8_t smem_raw[];
@@ -537,6 +668,13 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
+  if constexpr (wide_slow(BN, SLOW)) {
+    // 256-column slow tiles are planned without split-K or swapped operands.
+    if (p.splits != 1 || p.swap) {
+      if (threadIdx.x == 0) atomicOr(p.abort_word, kErrPlan);
+      return;
+    }
+  }
   // CG == 2: a cluster of two CTAs computes 256-row tiles with two-SM MMAs
   // issued by the leader (rank 0); each CTA stages its own 128 rows of X and
   // half of the Y tile, and holds its 128 rows of the accumulator in TMEM.
@@ -737,11 +875,11 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
   } else if (warp < EW) {
     // ------------------------------------------------------------ epilogue
     if (p.out_es == 4)
-      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 4, EW), 4>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 4, EW, wide_slow(BN, SLOW)), 4>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
                                                             lane);
     else
-      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 2, EW), 2>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 2, EW, wide_slow(BN, SLOW)), 2>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
                                                             lane);
   }

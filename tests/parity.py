@@ -41,15 +41,16 @@ def to_device(p: synth.Problem, device="cuda:0"):
     return (p.a.to(dev), p.b.to(dev), p.scale_a.to(dev), p.scale_b.to(dev))
 
 
-def run_gpu(p: synth.Problem, *, splitk=0, swap_ab=0, block_n=0, cta_pair=0, device="cuda:0", tensors=None):
+def run_gpu(p: synth.Problem, *, splitk=0, swap_ab=0, block_n=0, cta_pair=0, epi_warps=0, device="cuda:0",
+            tensors=None):
     """One fp8mm_run through the C ABI; returns (C on device [L][M][N], amax tensor, plan)."""
     a, b, sa, sb = tensors if tensors is not None else to_device(p, device)
     c, amax = pm.scaled_mm(a, b, sa, sb, out_dtype=synth.OUT_TORCH[p.out_dtype],
                            use_fast_accum=p.fast_accum, a_fmt=p.a_fmt, b_fmt=p.b_fmt,
                            scale_mode=p.scale_mode, splitk=splitk, swap_ab=swap_ab, block_n=block_n,
-                           cta_pair=cta_pair)
+                           cta_pair=cta_pair, epi_warps=epi_warps)
     key = (p.M, p.N, p.K, p.L, p.a_fmt, p.b_fmt, p.scale_mode, p.out_dtype, 1 if p.fast_accum else 0,
-           splitk, swap_ab, block_n, torch.device(device).index or 0, cta_pair)
+           splitk, swap_ab, block_n, torch.device(device).index or 0, cta_pair, epi_warps)
     return c, amax, pm.plan_for(key)
 
 

@@ -182,6 +182,25 @@ def test_cta_pair_tiles_ragged(fast, block_n):
     assert plan.info()["cta_pair"] == 1
 
 
+@pytest.mark.parametrize("epi_warps", [8, 16])
+@pytest.mark.parametrize("case", ["tensor_bf16", "tensor_f32", "tensor_f16", "block128", "block1", "block128_f32"])
+def test_slow_wide_tiles(case, epi_warps):
+    # slow accumulation on 256-column tiles: 128 promoted sums per epilogue thread,
+    # ragged in M, N (a last tile 8 columns wide) and K
+    if case.startswith("tensor"):
+        out = {"bf16": synth.OUT_BF16, "f32": synth.OUT_F32, "f16": synth.OUT_F16}[case.split("_")[1]]
+        p = synth.llm_per_tensor(M=300, N=520, K=640, seed=28, fast_accum=False, out_dtype=out)
+        if out == synth.OUT_F16:
+            p.scale_a.fill_(0.0625)
+            p.scale_b.fill_(0.5)
+    else:
+        p = synth.blockwise(M=300, N=520, K=640, seed=29, b_block=1 if case == "block1" else 128,
+                            out_dtype=synth.OUT_F32 if case.endswith("f32") else synth.OUT_BF16)
+    c, amax, plan = _run_check(p, block_n=256, swap_ab=2, epi_warps=epi_warps)
+    info = plan.info()
+    assert info["block_n"] == 256 and info["splitk"] == 1 and info["epi_warps"] == epi_warps
+
+
 def test_cta_pair_blockwise_and_split_k():
     p = synth.blockwise(M=384, N=264, K=1024, seed=25)
     c, amax, plan = _run_check(p, cta_pair=1, splitk=3, swap_ab=2)
