@@ -122,7 +122,7 @@ size_t layout(fp8mm_plan_s* P, int stages) {
   off += sf_bytes * stages;
   off = (off + 1023u) & ~1023u;
   P->off_out = off;
-  off += (uint32_t)(P->ew * stage_out_bytes(P->ew, wide_slow(P->bn, P->slow != 0)));
+  off += (uint32_t)(P->ew * stage_out_bytes(P->ew, held_tile(P->bn, P->slow != 0, P->mx != 0)));
   P->off_ys = off;
   // per-column Y scales of the current chunk, one row per epilogue warp
   if (P->x_kind != kScaleNone && P->y_kind == kScaleRow) off += (uint32_t)(P->ew * part_max_cols(P->bn, P->ew) * 4);
@@ -260,6 +260,8 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   }
   if (P->slow && bn > 128 && (bn != 256 || swap || mx || d.cta_pair == 1 || d.splitk > 1))
     return FP8MM_ERR_UNSUPPORTED;
+  // (a requested split needs the narrower MX tile: 256-column ones are held)
+  if (mx && !P->slow && bn == 256 && d.block_n == 0 && d.splitk > 1) bn = 128;
   // MX tiles must start on a 128-row factor atom: the block-scaled MMA reads
   // its factors from a TMEM column aligned to the atom's four columns.
   if (mx && bn != 128 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
@@ -291,9 +293,11 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   // are small next to the operand bytes they save.
   int S = d.splitk;
   const int64_t slots = P->sms / P->cg;  // concurrent work units (CTAs or CTA pairs)
+  const bool held = held_tile(bn, P->slow != 0, mx);
+  if (held && S > 1) return FP8MM_ERR_UNSUPPORTED;  // held tiles are never split
   if (S == 0) {
     S = 1;
-    if (!wide && tiles < 2 * slots && P->num_kb >= 8) {
+    if (!held && tiles < 2 * slots && P->num_kb >= 8) {
       double best = (double)tiles / (double)(cdiv(tiles, slots) * slots);
       for (int sk = 2; sk <= 8; ++sk) {
         if (P->num_kb / sk < 4) break;
@@ -519,7 +523,7 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   }
   // One TMA store per warp covers 32 tile rows x `cw` tile columns, staged in
   // shared memory with the swizzle that matches its row length.
-  const int cw = chunk_cols(P->bn, P->out_es, P->ew, wide_slow(P->bn, P->slow != 0));
+  const int cw = chunk_cols(P->bn, P->out_es, P->ew, held_tile(P->bn, P->slow != 0, P->mx != 0));
   uint32_t rowbytes;
   cuuint32_t cbox[3];
   if (!P->swap) {

@@ -53,6 +53,13 @@ __host__ __device__ constexpr int kernel_threads(int ew) { return (ew + 2) * 32;
 // output chunks are narrow (32 bytes of a row) and staged in half the
 // shared memory.
 __host__ __device__ constexpr bool wide_slow(int bn, bool slow) { return slow && bn > 128; }
+// Tiles whose epilogue holds the whole tile in registers before storing it:
+// slow 256-column tiles (the promoted sums) and MX 256-column tiles, whose
+// single TMEM accumulator is copied out and released at once so that the
+// next tile's MMAs overlap the stores.  Such tiles are never split or swapped.
+__host__ __device__ constexpr bool held_tile(int bn, bool slow, bool mx) {
+  return wide_slow(bn, slow) || (mx && !slow && bn == 256);
+}
 // Per-warp output staging: two buffers of 32 rows x 64 B (8 epilogue warps)
 // or 32 rows x 32 B (16 epilogue warps, or 256-column slow tiles).  (Rows of
 // 16 B measured far slower: the stores then write half sectors.)
@@ -299,7 +306,7 @@ __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap*
 // four for 16).  Per work unit: (slow) promote
 // each 128-K chunk into fp32 registers; (split-K) publish the partial tile and
 // let the last arrival finish it; then scale, cast, amax and store.
-template <int BN, bool SLOW, int CG, int EW, int CW, int ES>
+template <int BN, bool SLOW, int CG, int EW, int CW, int ES, bool HOLD>
 __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm_c, uint8_t* sgen, uint32_t sbase,
                                          uint32_t tmem_base, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t bar_epi,
                                          volatile uint32_t* misc, volatile uint32_t* abort_flag, uint32_t rank,
@@ -307,13 +314,14 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   constexpr int HMAX = part_max_cols(BN, EW);  // widest column range of a warp
   constexpr bool WIDE = wide_slow(BN, SLOW);     // 128 promoted sums per thread
   // columns per tcgen05.ld while promoting (16 beside 128 sums, within 168 registers)
-  constexpr int LDW = HMAX < 32 ? HMAX : (WIDE ? 16 : 32);
+  constexpr int LDW = HMAX < 32 ? HMAX : (HOLD ? 16 : 32);
+  static_assert(!WIDE || HOLD, "slow 256-column tiles hold their sums");
   static_assert(EW == 8 || EW == 16, "8 or 16 epilogue warps");
   static_assert(EW == 8 || BN % 128 == 0, "16 epilogue warps split 128-multiple tiles in four");
   static_assert(!SLOW || HMAX * (EW / 4) == BN, "slow accumulation splits the tile evenly");
-  static_assert(!WIDE || CG == 1, "256-column slow tiles run on one CTA");
+  static_assert(!HOLD || CG == 1, "held tiles run on one CTA");
   static_assert(HMAX % CW == 0 && (BN - HMAX) % CW == 0, "chunks tile each part");
-  constexpr int kStageOut = stage_out_bytes(EW, WIDE);
+  constexpr int kStageOut = stage_out_bytes(EW, HOLD);
   const int qd = warp & 3;
   const int h = warp >> 2;
   const int row = qd * 32 + lane;
@@ -334,9 +342,9 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   // on the narrower ones (which measured faster with scalar code).
   static_assert(HMAX % 2 == 0, "column ranges pair up");
   float acc1[(SLOW && !WIDE) ? HMAX : 1];
-  float2 acc2[WIDE ? HMAX / 2 : 1];
+  float2 acc2[HOLD ? HMAX / 2 : 1];
   auto acc = [&](int i) -> float& {
-    if constexpr (WIDE)
+    if constexpr (HOLD)
       return (i & 1) ? acc2[i >> 1].y : acc2[i >> 1].x;
     else
       return acc1[i];
@@ -516,6 +524,20 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
         break;
       }
       ptx::tc_fence_after_sync();
+      if constexpr (HOLD) {
+        // Copy the whole accumulator out and hand TMEM back to the MMA issuer
+        // before storing anything.
+        const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
+#pragma unroll
+        for (int pc = 0; pc < HMAX / 16; ++pc) {
+          uint32_t r[16];
+          tmem_load<16>(taddr + pc * 16, r);
+#pragma unroll
+          for (int i = 0; i < 16; i += 2)
+            acc2[(pc * 16 + i) / 2] = make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+        }
+        release_acc();
+      }
     }
     // Fast accumulation reads the finished tile from TMEM chunk by chunk.
     const uint32_t taddr = tmem_base + lane_off + abuf * BN + col0;
@@ -547,7 +569,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
     // ---------------------------------------------------- split-K fix-up
     bool finish = true;
     float* tile_ws = nullptr;
-    if (!WIDE && p.splits > 1) {  // (256-column slow tiles are never split)
+    if (!HOLD && p.splits > 1) {  // (held tiles are never split)
       const long long tile = (((long long)t.l * p.tiles_r + t.tr) * p.tiles_q + t.tq) * CG + rank;
       tile_ws = p.ws_partials + (size_t)tile * p.splits * (kBlockM * BN);
       float* slot = tile_ws + (size_t)t.s * (kBlockM * BN);
@@ -588,8 +610,8 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
     if (finish) {
       const int r0 = xbase + qd * 32;  // X row of the warp's first lane
       auto finish_chunk = [&](int ci) {
-        if constexpr (WIDE) {
-          // The promoted sums are stored in place: the chunk is acc[0 .. CW),
+        if constexpr (HOLD) {
+          // The held sums are stored in place: the chunk is acc[0 .. CW),
           // then the others move down by CW.
           const int q0 = t.tq * BN + col0 + ci * CW;
           float v[CW];
@@ -639,7 +661,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
 #pragma unroll 1
       for (int ci = 0; ci < nch; ++ci) finish_chunk(ci);
     }
-    if constexpr (!SLOW) release_acc();
+    if constexpr (!SLOW && !HOLD) release_acc();
   }
   if (lane == 0) ptx::bulk_wait_all();
   uint32_t amax_local = amax_nan ? 0x7FFFFFFFu : __float_as_uint(amax_f);
@@ -668,8 +690,8 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
-  if constexpr (wide_slow(BN, SLOW)) {
-    // 256-column slow tiles are planned without split-K or swapped operands.
+  if constexpr (held_tile(BN, SLOW, MX)) {
+    // Held tiles are planned without split-K or swapped operands.
     if (p.splits != 1 || p.swap) {
       if (threadIdx.x == 0) atomicOr(p.abort_word, kErrPlan);
       return;
@@ -875,11 +897,11 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
   } else if (warp < EW) {
     // ------------------------------------------------------------ epilogue
     if (p.out_es == 4)
-      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 4, EW, wide_slow(BN, SLOW)), 4>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 4, EW, held_tile(BN, SLOW, MX)), 4, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
                                                             lane);
     else
-      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 2, EW, wide_slow(BN, SLOW)), 2>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 2, EW, held_tile(BN, SLOW, MX)), 2, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
                                                             lane);
   }
