@@ -17,6 +17,7 @@ KernelFn kernel_bn192_fast_f8_cg1_ew8();
 KernelFn kernel_bn224_fast_f8_cg1_ew8();
 KernelFn kernel_bn256_fast_f8_cg1_ew8();
 KernelFn kernel_bn256_fast_f8_cg2_ew8();
+KernelFn kernel_bn224_fast_f8_cg2_ew8();
 KernelFn kernel_bn128_fast_f8_cg2_ew8();
 KernelFn kernel_bn128_slow_f8_cg2_ew8();
 KernelFn kernel_bn128_slow_f8_cg1_ew8();
@@ -45,6 +46,7 @@ inline const KernelEntry* kernel_table(int* n) {
       {224, 0, 0, 1, 8, &kernel_bn224_fast_f8_cg1_ew8},
       {256, 0, 0, 1, 8, &kernel_bn256_fast_f8_cg1_ew8},
       {256, 0, 0, 2, 8, &kernel_bn256_fast_f8_cg2_ew8},
+      {224, 0, 0, 2, 8, &kernel_bn224_fast_f8_cg2_ew8},
       {128, 0, 0, 2, 8, &kernel_bn128_fast_f8_cg2_ew8},
       {128, 1, 0, 2, 8, &kernel_bn128_slow_f8_cg2_ew8},
       {128, 1, 0, 1, 8, &kernel_bn128_slow_f8_cg1_ew8},

@@ -174,7 +174,7 @@ def test_launch_count_is_one_kernel():
     assert plan.kernel_launches() == 1
 
 
-@pytest.mark.parametrize("fast,block_n", [(True, 256), (True, 128), (False, 128)])
+@pytest.mark.parametrize("fast,block_n", [(True, 256), (True, 224), (True, 128), (False, 128)])
 def test_cta_pair_tiles_ragged(fast, block_n):
     # two-SM MMAs: 256-row tiles split over a CTA pair, ragged in M, N and K
     p = synth.llm_per_tensor(M=520, N=392, K=640, seed=24, fast_accum=fast)
