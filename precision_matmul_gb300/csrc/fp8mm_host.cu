@@ -298,6 +298,18 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   P->ew = d.epi_warps ? d.epi_warps : ((P->slow && !mx && bn == 128 && P->cg == 1) || wide_ycol ? 16 : 8);
   KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
+  if (held_tile(bn, P->slow != 0, mx)) {
+    // The warpgroup register split only redistributes what the block was
+    // launched with; refuse the plan if the compiled kernel holds fewer
+    // registers per thread than the split hands out (its raise would wait
+    // forever).
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, (const void*)fn) != cudaSuccess) {
+      cudaGetLastError();
+      return FP8MM_ERR_CUDA;
+    }
+    if (fa.numRegs * (P->ew + 4) < P->ew * epi_regs(P->ew) + 4 * kRegRoles) return FP8MM_ERR_UNSUPPORTED;
+  }
 
   const int64_t tiles_r = std::max<int64_t>(1, cdiv(P->R, (int64_t)kBlockM * P->cg));
   const int64_t tiles_q = std::max<int64_t>(1, cdiv(P->Q, bn));
@@ -344,10 +356,11 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   if (d.stages > 0) {
     if (d.stages > stages) return FP8MM_ERR_UNSUPPORTED;
     stages = d.stages;
-  } else if (wide) {
-    // Slow 256-column tiles keep a shallow ring: the shared memory left over
-    // becomes L1 for their scale loads and register spills, which measured
-    // faster on GB300 than a deeper ring (3 stages, 2 with per-column scales).
+  } else if (wide && blockwise) {
+    // Block-scaled slow 256-column tiles keep a shallow ring: the shared
+    // memory left over becomes L1 for their per-chunk scale loads, which
+    // measured faster on GB300 than a deeper ring (3 stages, 2 with
+    // per-column scales).
     stages = std::min(stages, wide_ycol ? 2 : 3);
   }
   // Slow accumulation hands each 128-K chunk to the epilogue: with 128-column
@@ -382,7 +395,7 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)P->grid);
-    cfg.blockDim = dim3(kernel_threads(P->ew));
+    cfg.blockDim = dim3(kernel_threads(P->ew, held_tile(P->bn, P->slow != 0, P->mx != 0)));
     cfg.dynamicSmemBytes = P->smem_bytes;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -650,7 +663,7 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)P->grid);
-  cfg.blockDim = dim3(kernel_threads(P->ew));
+  cfg.blockDim = dim3(kernel_threads(P->ew, held_tile(P->bn, P->slow != 0, P->mx != 0)));
   cfg.dynamicSmemBytes = P->smem_bytes;
   cfg.stream = stream;
   cfg.attrs = attr;

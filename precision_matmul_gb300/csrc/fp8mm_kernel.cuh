@@ -46,8 +46,23 @@ constexpr int kUmmaK = 32;        // K per tcgen05.mma for 8-bit operands
 // Bound on one wait: 2^31 SM clock cycles, about one second at GB300 clocks.
 constexpr uint64_t kWaitLimitCycles = 1ull << 31;
 
-// Block geometry shared by the kernel and the host planner.
-__host__ __device__ constexpr int kernel_threads(int ew) { return (ew + 2) * 32; }
+// Block geometry shared by the kernel and the host planner: EW epilogue
+// warps, the producer and the MMA issuer, and (for held tiles) two idle warps
+// that complete the last warpgroup of the register split below.
+__host__ __device__ constexpr int kernel_threads(int ew, bool held) { return (ew + (held ? 4 : 2)) * 32; }
+// Held tiles split the register file by warpgroup (setmaxnreg): the
+// producer/MMA warpgroup drops to kRegRoles so that the epilogue warps,
+// which keep a whole tile row range in registers, rise to epi_regs(ew).
+// Launch cap: 12 warps -> 3 per SM sub-partition -> 168; 20 warps -> 5 -> 96.
+constexpr int kRegRoles = 64;
+__host__ __device__ constexpr int launch_regs(int ew) { return ew == 8 ? 168 : 96; }
+__host__ __device__ constexpr int epi_regs(int ew) { return ew == 8 ? 216 : 104; }
+// Each sub-partition holds EW/4 epilogue warps and one warp of the last group.
+static_assert(2 * epi_regs(8) + kRegRoles <= 512 && 4 * epi_regs(16) + kRegRoles <= 512,
+              "register split per SM sub-partition");
+static_assert((8 * epi_regs(8) + 4 * kRegRoles) <= 12 * launch_regs(8) &&
+                  (16 * epi_regs(16) + 4 * kRegRoles) <= 20 * launch_regs(16),
+              "register split within the launch's allocation");
 // Slow accumulation on 256-column tiles: each epilogue warp keeps 128 (8
 // warps) or 64 (16 warps) promoted fp32 sums per row in registers, so its
 // output chunks are narrow (32 bytes of a row) and staged in half the
@@ -671,7 +686,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
 }
 
 template <int BN, bool SLOW, bool MX, int CG, int EW>
-__global__ void __launch_bounds__(kernel_threads(EW), 1)
+__global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1)
     fp8mm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                  const __grid_constant__ CUtensorMap tm_c, const KParams p) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
@@ -747,8 +762,10 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
   const uint32_t tmem_base = misc[0];
   volatile uint32_t* abort_flag = misc + 1;
 
+  constexpr bool REGSPLIT = held_tile(BN, SLOW, MX);
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
+    if constexpr (REGSPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegRoles));
     if (lane == 0) {
       ptx::prefetch_tensormap(&tm_x);
       ptx::prefetch_tensormap(&tm_y);
@@ -816,6 +833,7 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    if constexpr (REGSPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegRoles));
     if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
       bool ok = true;
@@ -896,6 +914,7 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
     }
   } else if (warp < EW) {
     // ------------------------------------------------------------ epilogue
+    if constexpr (REGSPLIT) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(epi_regs(EW)));
     if (p.out_es == 4)
       epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 4, EW, held_tile(BN, SLOW, MX)), 4, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
@@ -904,6 +923,9 @@ __global__ void __launch_bounds__(kernel_threads(EW), 1)
       epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 2, EW, held_tile(BN, SLOW, MX)), 2, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
                                                             lane);
+  } else {
+    // the idle warps of the last warpgroup give their registers up too
+    if constexpr (REGSPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegRoles));
   }
 
   ptx::tc_fence_before_sync();
