@@ -291,11 +291,10 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     P->cg = 2;
   }
   // Epilogue warps: 16 for slow accumulation at 128 columns (more TMEM loads
-  // in flight during the per-chunk promotion) and for slow 256-column tiles
-  // with per-column Y scales (their per-chunk scale work spread wider), else 8.
+  // in flight during the per-chunk promotion), else 8.
   const bool wide = wide_slow(bn, P->slow != 0);
   const bool wide_ycol = wide && blockwise && P->y_kind == kScaleRow;
-  P->ew = d.epi_warps ? d.epi_warps : ((P->slow && !mx && bn == 128 && P->cg == 1) || wide_ycol ? 16 : 8);
+  P->ew = d.epi_warps ? d.epi_warps : ((P->slow && !mx && bn == 128 && P->cg == 1) ? 16 : 8);
   KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
   if (held_tile(bn, P->slow != 0, mx)) {
