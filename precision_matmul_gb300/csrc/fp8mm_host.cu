@@ -201,13 +201,15 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   P->slow = (blockwise || !d.fast_accum) ? 1 : 0;
 
   // Swap-AB for skinny M: the long N side then fills the 128-lane MMA M side.
+  // (From 129 to 256 rows unswapped 256-row pair tiles, or slow 256-column
+  // tiles, measured 13-17% faster on GB300 than swapped ones.)
   bool swap;
   if (d.swap_ab == 1)
     swap = true;
   else if (d.swap_ab == 2)
     swap = false;
   else
-    swap = !mx && d.M <= 256 && d.N > d.M;
+    swap = !mx && d.M <= 128 && d.N > d.M;
   P->swap = swap ? 1 : 0;
   P->R = swap ? d.N : d.M;
   P->Q = swap ? d.M : d.N;

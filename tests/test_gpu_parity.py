@@ -84,7 +84,7 @@ def test_mx_wide_tiles(fmt):
     assert plan.info()["block_n"] == 256
 
 
-@pytest.mark.parametrize("M", [16, 40, 64, 200])
+@pytest.mark.parametrize("M", [16, 40, 64, 120])
 @pytest.mark.parametrize("data", ["gauss40", "adversarial"])
 @pytest.mark.parametrize("fast", [True, False])
 def test_skinny_swap_ab_split_k(M, data, fast):
@@ -92,6 +92,14 @@ def test_skinny_swap_ab_split_k(M, data, fast):
     c, amax, plan = _run_check(p)
     info = plan.info()
     assert info["swap_ab"] == 1
+
+
+@pytest.mark.parametrize("fast", [True, False])
+def test_skinny_200_rows_unswapped(fast):
+    # 129..256 rows run unswapped (pair tiles when fast, 256-column tiles when slow)
+    p = synth.skinny(M=200, N=1536, K=2048, data="gauss40", seed=30, fast_accum=fast)
+    c, amax, plan = _run_check(p)
+    assert plan.info()["swap_ab"] == 0
 
 
 @pytest.mark.parametrize("splitk", [2, 3, 5])
