@@ -138,7 +138,7 @@ size_t layout(fp8mm_plan_s* P, int stages) {
 double width_efficiency(int bn, bool mx) {
   switch (bn) {
     case 256: return mx ? 0.85 : 1.0;  // the MX form keeps one accumulator at 256 columns
-    case 224: return 0.97;
+    case 224: return mx ? 0.80 : 0.97;  // MX: factors gathered per stage, fp32 stores beside the mainloop
     case 192: return 0.93;
     default: return 0.6;
   }
@@ -266,7 +266,7 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
       // (under one wave of 256-wide tiles the widest tile is the fastest)
       double best = 1e300;
       for (int c : {256, 224, 192, 128}) {
-        if (mx && c != 256 && c != 128) continue;
+        if (mx && c == 192) continue;
         const int64_t tiles = tiles_r1 * cdiv(P->Q, c) * L;
         const double cost = (double)cdiv(tiles, P->sms) * c / width_efficiency(c, mx);
         if (cost < best * 0.999) {
@@ -283,9 +283,10 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     return FP8MM_ERR_UNSUPPORTED;
   // (a requested split needs the narrower MX tile: 256-column ones are held)
   if (mx && !P->slow && bn == 256 && d.block_n == 0 && d.splitk > 1) bn = 128;
-  // MX tiles must start on a 128-row factor atom: the block-scaled MMA reads
-  // its factors from a TMEM column aligned to the atom's four columns.
-  if (mx && bn != 128 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
+  // MX tiles are 128 or 256 columns, or 224: the block-scaled MMA reads its
+  // factors from a TMEM column aligned to an atom's four columns, so the
+  // 224-column kernel rebuilds Y's atoms to start at the tile's first row.
+  if (mx && bn != 128 && bn != 224 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
   P->bn = bn;
 
   if (d.cta_pair == 1 || auto_pair) {

@@ -4,5 +4,6 @@
 namespace fp8mm {
 
 KernelFn kernel_bn128_fast_mx_cg1_ew8() { return &fp8mm_kernel<128, false, true, 1, 8>; }
+KernelFn kernel_bn224_fast_mx_cg1_ew8() { return &fp8mm_kernel<224, false, true, 1, 8>; }
 
 }  // namespace fp8mm

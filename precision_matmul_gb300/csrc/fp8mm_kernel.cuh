@@ -89,8 +89,9 @@ __host__ __device__ constexpr int chunk_cols(int bn, int es, int ew, bool ws) {
             : (((ew == 8 ? 64 : 32) / es) < part_max_cols(bn, ew) ? ((ew == 8 ? 64 : 32) / es)
                                                                    : part_max_cols(bn, ew));
 }
-// MX: shared-memory bytes per stage for the factor atoms (X's atom and up to
-// three of Y's when the tile is not aligned to 128 rows).
+// MX: shared-memory bytes per stage for the factor atoms: X's atom and up to
+// three of Y's (a 256-column tile copies whole atoms; a 224-column one has two
+// atoms gathered to start at the tile's first row).
 constexpr uint32_t kSfStageBytes = 2048;
 
 // Abort codes (OR-ed into the device word).
@@ -690,7 +691,8 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
     fp8mm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                  const __grid_constant__ CUtensorMap tm_c, const KParams p) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
-  static_assert(!MX || BN == 128 || BN == 256, "MX tiles start on a 128-row factor atom");
+  static_assert(!MX || BN == 128 || BN == 256 || (BN % 32 == 0 && BN < 256),
+                "MX tiles start on a 32-row boundary of a factor atom");
   static_assert(!SLOW || BN <= 128 || (BN == 256 && CG == 1 && !MX),
                 "slow accumulation keeps its promoted sums in registers: 256-column tiles on one CTA");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
@@ -701,6 +703,11 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
   uint8_t* sgen = smem_raw + (sbase - sraw);
 
   constexpr int kProdWarp = EW;
+  // MX tiles not aligned to 128 rows (224 columns): the producer warp gathers
+  // Y's factor bytes into atoms that start at the tile's first row, with
+  // 4-byte asynchronous copies whose completion the stage's full barrier
+  // tracks (one arrival per lane besides the producer's).
+  constexpr bool GATHER = MX && (BN % 128) != 0;
   constexpr int kMmaWarp = EW + 1;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -731,7 +738,7 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(bar_full + 8u * s, 1);
+      ptx::mbar_init(bar_full + 8u * s, GATHER ? 33 : 1);
       ptx::mbar_init(bar_empty + 8u * s, 1);
     }
     for (int b = 0; b < 4; ++b) {
@@ -766,10 +773,12 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
     if constexpr (REGSPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegRoles));
-    if (lane == 0) {
-      ptx::prefetch_tensormap(&tm_x);
-      ptx::prefetch_tensormap(&tm_y);
-      ptx::prefetch_tensormap(&tm_c);
+    if (GATHER || lane == 0) {
+      if (lane == 0) {
+        ptx::prefetch_tensormap(&tm_x);
+        ptx::prefetch_tensormap(&tm_y);
+        ptx::prefetch_tensormap(&tm_c);
+      }
       uint32_t stage = 0, phase = 0;
       long long narm = 0;
       bool ok = true;
@@ -781,14 +790,19 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
         const int yrow0 = t.tq * BN + (int)rank * (BN / CG);
         // MX: Y's tile may start inside a 128-row atom; copy every atom it touches.
         const int y_atom0 = (t.tq * BN) / 128;
-        const int y_atoms = MX ? ((t.tq * BN) % 128 + BN + 127) / 128 : 0;
+        const int y_atoms = (MX && !GATHER) ? ((t.tq * BN) % 128 + BN + 127) / 128 : 0;
         const uint32_t tx = CG * (p.x_stage_bytes + p.y_stage_bytes) + (MX ? 512u * (1 + y_atoms) : 0u);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
-          if (!wait_bar(bar_empty + 8u * stage, phase ^ 1u, abort_flag, p.abort_word, kErrProducer)) {
-            ok = false;
-            break;
+          {
+            bool w = wait_bar(bar_empty + 8u * stage, phase ^ 1u, abort_flag, p.abort_word, kErrProducer);
+            if constexpr (GATHER) w = __all_sync(0xFFFFFFFFu, w);  // the lanes leave together
+            if (!w) {
+              ok = false;
+              break;
+            }
           }
           const uint32_t fb = bar_full + 8u * stage;
+          if (!GATHER || lane == 0) {
           if constexpr (CG == 2) {
             const uint32_t fb_leader = ptx::mapa_shared(fb, 0u);
             if (leader) ptx::mbar_arrive_expect_tx(fb, tx);
@@ -813,6 +827,26 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
               ptx::bulk_load(sf + 512u * (1 + i), gy, 512u, fb);
             }
           }
+          }  // (lane 0)
+          if constexpr (GATHER) {
+            // Gathered atom v, line `lane`, word c: the factors of tile row
+            // 128 v + 32 c + lane, which sit in word (row % 128) / 32 of line
+            // row % 32 (= lane: tiles start on a 32-row boundary) of the row's
+            // atom.  Atoms past the last row block are clamped to it.
+            const uint32_t sf = sbase + p.off_sf + stage * p.sf_stage_bytes;
+#pragma unroll
+            for (int v = 0; v < (BN + 127) / 128; ++v) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int row = t.tq * BN + 128 * v + 32 * c + lane;
+                const int mb = min(row / 128, p.sfy_mb - 1);
+                const uint8_t* src = p.sfy + (((size_t)t.l * p.sfy_mb + mb) * p.scale_kb + kb) * 512u +
+                                     (uint32_t)lane * 16u + (uint32_t)((row % 128) / 32) * 4u;
+                ptx::cp_async_4(sf + 512u * (1 + v) + (uint32_t)lane * 16u + (uint32_t)c * 4u, src);
+              }
+            }
+            ptx::cp_async_mbar_arrive_noinc(fb);
+          }
           ++narm;
           if (++stage == (uint32_t)S) {
             stage = 0;
@@ -825,7 +859,7 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
       // (stage, phase) is the next slot: slots below it were last armed in
       // this pass of the ring, the others in the previous pass.  With a CTA
       // pair the leader's barriers also track the peer's copies.
-      if (leader) {
+      if (leader && lane == 0) {
         for (int s = 0; s < S; ++s) {
           if (narm > s) drain_wait(bar_full + 8u * s, ((uint32_t)s < stage) ? phase : (phase ^ 1u), p.abort_word);
         }
@@ -859,13 +893,14 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
           const uint64_t bdesc = ptx::desc_sw128_kmajor(sbase + p.off_y + stage * p.y_stage_bytes);
           if constexpr (MX) {
             const uint32_t sf_smem = sbase + p.off_sf + stage * p.sf_stage_bytes;
+            const uint32_t sf_x = tmem_base + (uint32_t)(p.num_acc * BN) + stage * 16u;
             // TMEM slot of 16 columns per stage: X's atom in columns 0-3, Y's
             // atoms from column 4.  Row r of an atom sits in lane r % 32 of
             // column r / 32, so a Y tile starting at row o of its first atom
-            // reads its factors from column 4 + o / 32 on.
-            const uint32_t sf_x = tmem_base + (uint32_t)(p.num_acc * BN) + stage * 16u;
-            const int y_atoms = ((t.tq * BN) % 128 + BN + 127) / 128;
-            const uint32_t sf_y = sf_x + 4u + (uint32_t)(((t.tq * BN) % 128) / 32);
+            // reads its factors from column 4 + o / 32 on; gathered atoms
+            // (224-column tiles) start at the tile's first row: column 4.
+            const int y_atoms = GATHER ? (BN + 127) / 128 : ((t.tq * BN) % 128 + BN + 127) / 128;
+            const uint32_t sf_y = sf_x + 4u + (GATHER ? 0u : (uint32_t)(((t.tq * BN) % 128) / 32));
             ptx::tmem_cp_32x128b_warpx4(sf_x, ptx::desc_sf_atom(sf_smem));
             for (int i = 0; i < y_atoms; ++i)
               ptx::tmem_cp_32x128b_warpx4(sf_x + 4u + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * (1 + i)));

@@ -25,6 +25,7 @@ KernelFn kernel_bn128_slow_f8_cg1_ew16();
 KernelFn kernel_bn256_slow_f8_cg1_ew8();
 KernelFn kernel_bn256_slow_f8_cg1_ew16();
 KernelFn kernel_bn128_fast_mx_cg1_ew8();
+KernelFn kernel_bn224_fast_mx_cg1_ew8();
 KernelFn kernel_bn256_fast_mx_cg1_ew8();
 KernelFn kernel_bn128_slow_mx_cg1_ew8();
 
@@ -54,6 +55,7 @@ inline const KernelEntry* kernel_table(int* n) {
       {256, 1, 0, 1, 8, &kernel_bn256_slow_f8_cg1_ew8},
       {256, 1, 0, 1, 16, &kernel_bn256_slow_f8_cg1_ew16},
       {128, 0, 1, 1, 8, &kernel_bn128_fast_mx_cg1_ew8},
+      {224, 0, 1, 1, 8, &kernel_bn224_fast_mx_cg1_ew8},
       {256, 0, 1, 1, 8, &kernel_bn256_fast_mx_cg1_ew8},
       {128, 1, 1, 1, 8, &kernel_bn128_slow_mx_cg1_ew8},
   };

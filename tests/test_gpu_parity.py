@@ -84,6 +84,15 @@ def test_mx_wide_tiles(fmt):
     assert plan.info()["block_n"] == 256
 
 
+@pytest.mark.parametrize("fmt", [synth.E4M3, synth.E5M2])
+def test_mx_224_tiles_every_atom_shift(fmt):
+    # 224-column tiles start at 0, 96, 64 and 32 rows into a 128-row factor
+    # atom (columns 0, 224, 448, 672); the kernel rebuilds Y's atoms per tile
+    p = synth.mx_batched(L=2, M=264, N=904, K=384, fmt=fmt, seed=36)
+    c, amax, plan = _run_check(p, block_n=224)
+    assert plan.info()["block_n"] == 224
+
+
 @pytest.mark.parametrize("M", [16, 40, 64, 120])
 @pytest.mark.parametrize("data", ["gauss40", "adversarial"])
 @pytest.mark.parametrize("fast", [True, False])
