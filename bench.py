@@ -210,6 +210,23 @@ def oracle_sample(probs, target_s=8.0, max_rows=None):
     return total_flops / total_t / 1e12, threads, "; ".join(descr)
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (every rank gets it); x itself on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, step_s: float, world: int) -> float:
+    """Replicas: every rank does the same work per step; the job's rate is
+    all ranks' work over the slowest rank's step time."""
+    return world * flops_per_rank / step_s / 1e12
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -294,13 +311,9 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     for i, e0, e1 in evs:
         per_call[i].append(e0.elapsed_time(e1) / 1e3)
-    step_s = sum(sum(x) for x in per_call) / args.steps
-    if world > 1:
-        t = torch.tensor([step_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_s = float(t.item())
+    step_s = max_over_ranks(sum(sum(x) for x in per_call) / args.steps, world, dev)
     flops = sum(p.flops for p in probs)
-    value = world * flops / step_s / 1e12
+    value = whole_job_tflops(flops, step_s, world)
     err = pm.fp8mm_device_error(local_rank)
     if err:
         raise SystemExit(f"device abort recorded: {err:#x}")
