@@ -14,17 +14,23 @@
 // for skinny M the roles swap (X = B, Y = A) and the epilogue stores the
 // tile transposed, so that the long dimension fills the 128-row side.
 //
-// Roles ((EW + 2) warps, one CTA per SM, persistent over work units):
+// Roles ((EW + 2) warps, or EW + 4 for held tiles; one CTA per SM, or a
+// cluster of two CTAs per 256-row tile; persistent over work units):
 //   warps 0..EW-1  epilogue (EW = 8 or 16): TMEM -> registers; for slow
 //              accumulation and block scales, one promotion per 128-K chunk
 //              (acc += s_x s_y chunk in fp32); split-K fix-up; scale, cast,
 //              NaN canonicalisation, amax, shared-memory staging, TMA stores.
 //   warp EW    TMA producer: A/B tiles (128 B of K per row, 128-byte swizzle)
-//              and, for the MX form, the 512-byte scale-factor atoms, into a
-//              ring of `stages` shared-memory slots guarded by mbarriers.
-//   warp EW+1  MMA issuer: tcgen05.mma kind::f8f6f4 (or kind::mxf8f6f4 with
-//              block scaling) into one or two TMEM accumulators; also owns
-//              the TMEM allocation.
+//              and, for the MX form, the 512-byte scale-factor atoms (for
+//              224-column tiles gathered by the whole warp to start at the
+//              tile), into a ring of `stages` shared-memory slots guarded by
+//              mbarriers.
+//   warp EW+1  MMA issuer: tcgen05.mma kind::f8f6f4 (cta_group::1, or
+//              cta_group::2 over a CTA pair) or kind::mxf8f6f4 with block
+//              scaling, into up to four TMEM accumulators; also owns the TMEM
+//              allocation.
+//   warps EW+2, EW+3  (held tiles only) idle: they complete the last
+//              warpgroup, which hands registers to the epilogue (setmaxnreg).
 //
 // Every wait on an mbarrier is bounded in time: when a limit is hit the
 // kernel records an error code in a device word, the other roles leave their
