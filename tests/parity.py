@@ -114,10 +114,12 @@ def check(p: synth.Problem, c: torch.Tensor, amax: torch.Tensor, *, rows=None, o
     if full_amax:
         assert got_amax_bits == amax_bits_of(c), (hex(got_amax_bits), hex(amax_bits_of(c)))
     if rows is None:
-        # within the bound of the oracle's max |C_exact|
-        ce_all = oracle.scaled_gemm(a, b, sa, sb, a_fmt=p.a_fmt, b_fmt=p.b_fmt, scale_mode=p.scale_mode,
-                                    out_dtype=p.out_dtype, nthreads=oracle_threads)[0]
-        if np.isfinite(ce_all).all():
+        # within the bound of the oracle's max |C_exact| (when every stored value is finite: an
+        # exact value that rounds to +-Inf in out_dtype makes amax +Inf on both sides)
+        ce_all, co_all, _ = oracle.scaled_gemm(a, b, sa, sb, a_fmt=p.a_fmt, b_fmt=p.b_fmt,
+                                               scale_mode=p.scale_mode, out_dtype=p.out_dtype,
+                                               nthreads=oracle_threads)
+        if np.isfinite(co_all).all():
             am = float(amax.item())
             assert abs(am - float(np.abs(ce_all).max())) <= global_tol + 1e-300
     return worst
