@@ -70,9 +70,7 @@ static_assert((8 * epi_regs(8) + 4 * kRegRoles) <= 12 * launch_regs(8) &&
                   (16 * epi_regs(16) + 4 * kRegRoles) <= 20 * launch_regs(16),
               "register split within the launch's allocation");
 // Slow accumulation on 256-column tiles: each epilogue warp keeps 128 (8
-// warps) or 64 (16 warps) promoted fp32 sums per row in registers, so its
-// output chunks are narrow (32 bytes of a row) and staged in half the
-// shared memory.
+// warps) or 64 (16 warps) promoted fp32 sums per row in registers.
 __host__ __device__ constexpr bool wide_slow(int bn, bool slow) { return slow && bn > 128; }
 // Tiles whose epilogue holds the whole tile in registers before storing it:
 // slow 256-column tiles (the promoted sums) and MX 256-column tiles, whose
@@ -82,16 +80,17 @@ __host__ __device__ constexpr bool held_tile(int bn, bool slow, bool mx) {
   return wide_slow(bn, slow) || (mx && !slow && bn == 256);
 }
 // Per-warp output staging: two buffers of 32 rows x 64 B (8 epilogue warps)
-// or 32 rows x 32 B (16 epilogue warps, or 256-column slow tiles).  (Rows of
-// 16 B measured far slower: the stores then write half sectors.)
-__host__ __device__ constexpr int stage_out_bytes(int ew, bool ws) { return (ew == 8 && !ws) ? 4096 : 2048; }
+// or 32 rows x 32 B (16 epilogue warps, or held tiles, whose registers leave
+// less room).  (Rows of 16 B measured far slower: the stores then write half
+// sectors.)
+__host__ __device__ constexpr int stage_out_bytes(int ew, bool held) { return (ew == 8 && !held) ? 4096 : 2048; }
 // Columns [0, half0_cols) belong to epilogue warps 0-3, the rest to warps 4-7.
 __host__ __device__ constexpr int half0_cols(int bn) { return bn <= 64 ? bn / 2 : ((bn / 2 + 31) / 32) * 32; }
 // Widest column range of one epilogue warp.
 __host__ __device__ constexpr int part_max_cols(int bn, int ew) { return ew == 8 ? half0_cols(bn) : bn / 4; }
 // Columns of one output chunk (one TMA store of 32 tile rows).
-__host__ __device__ constexpr int chunk_cols(int bn, int es, int ew, bool ws) {
-  return ws ? 32 / es
+__host__ __device__ constexpr int chunk_cols(int bn, int es, int ew, bool held) {
+  return held ? 32 / es
             : (((ew == 8 ? 64 : 32) / es) < part_max_cols(bn, ew) ? ((ew == 8 ? 64 : 32) / es)
                                                                    : part_max_cols(bn, ew));
 }
@@ -334,8 +333,8 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
                                          volatile uint32_t* misc, volatile uint32_t* abort_flag, uint32_t rank,
                                          long long u_first, long long u_step, int warp, int lane) {
   constexpr int HMAX = part_max_cols(BN, EW);  // widest column range of a warp
-  constexpr bool WIDE = wide_slow(BN, SLOW);     // 128 promoted sums per thread
-  // columns per tcgen05.ld while promoting (16 beside 128 sums, within 168 registers)
+  constexpr bool WIDE = wide_slow(BN, SLOW);     // slow 256-column tile: HMAX promoted sums per thread
+  // columns per tcgen05.ld while promoting (held tiles: 16, measured faster than 8 or 32)
   constexpr int LDW = HMAX < 32 ? HMAX : (HOLD ? 16 : 32);
   static_assert(!WIDE || HOLD, "slow 256-column tiles hold their sums");
   static_assert(EW == 8 || EW == 16, "8 or 16 epilogue warps");
