@@ -285,7 +285,7 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   if (mx && !P->slow && bn == 256 && d.block_n == 0 && d.splitk > 1) bn = 128;
   // MX tiles are 128 or 256 columns, or 224: the block-scaled MMA reads its
   // factors from a TMEM column aligned to an atom's four columns, so the
-  // 224-column kernel rebuilds Y's atoms to start at the tile's first row.
+  // 224-column kernel gathers Y's factor atoms to start at the tile's first row.
   if (mx && bn != 128 && bn != 224 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
   P->bn = bn;
 
