@@ -143,6 +143,15 @@ fp8mm_status fp8mm_plan_roofline(const fp8mm_plan_t* plan, double* flops, double
 
 fp8mm_status fp8mm_plan_get_info(const fp8mm_plan_t* plan, fp8mm_plan_info* info);
 
+/* What fp8mm_plan would choose for a device with `sms` SMs and
+ * `max_smem_bytes` of opt-in shared memory per block, without touching CUDA
+ * (no device query, no kernel attribute or occupancy query: CTA-pair grids
+ * assume one pair per two SMs, and the held kernels' register check is left
+ * out).  For tests and planning tools; fp8mm_plan stays authoritative.
+ * FP8MM_ERR_INVALID for sms < 2 or max_smem_bytes <= 0, else as fp8mm_plan. */
+fp8mm_status fp8mm_plan_preview(const fp8mm_desc* desc, int32_t sms, int32_t max_smem_bytes,
+                                fp8mm_plan_info* info);
+
 void fp8mm_destroy(fp8mm_plan_t* plan);
 
 /* Static string naming a status code. */

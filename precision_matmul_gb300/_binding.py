@@ -24,7 +24,7 @@ FP8MM_ERR_REJECTED, FP8MM_ERR_WORKSPACE, FP8MM_ERR_CUDA, FP8MM_ERR_DEVICE = 4, 5
 # Every symbol include/fp8mm.h declares.
 EXPORTS = ("fp8mm_plan", "fp8mm_workspace_size", "fp8mm_run", "fp8mm_plan_roofline",
            "fp8mm_plan_get_info", "fp8mm_destroy", "fp8mm_status_string", "fp8mm_device_error",
-           "fp8mm_plan_kernel_launches", "fp8mm_gemm", "fp8mm_run_static_workspace")
+           "fp8mm_plan_kernel_launches", "fp8mm_gemm", "fp8mm_run_static_workspace", "fp8mm_plan_preview")
 FP8MM_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 
@@ -84,6 +84,8 @@ def load():
     lib.fp8mm_gemm.restype = i32
     lib.fp8mm_run_static_workspace.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     lib.fp8mm_run_static_workspace.restype = i32
+    lib.fp8mm_plan_preview.argtypes = [ctypes.POINTER(fp8mm_desc), i32, i32, ctypes.POINTER(fp8mm_plan_info)]
+    lib.fp8mm_plan_preview.restype = i32
     _lib = lib
     return lib
 
@@ -183,3 +185,13 @@ def fp8mm_run_static_workspace(plan: Plan, a_ptr, b_ptr, sa_ptr, sb_ptr, c_ptr, 
     allocates nothing; see include/fp8mm.h for the sharing rules."""
     st = load().fp8mm_run_static_workspace(plan.handle, a_ptr, b_ptr, sa_ptr, sb_ptr, c_ptr, amax_ptr, stream)
     _check(st, "fp8mm_run_static_workspace")
+
+
+def fp8mm_plan_preview(desc: fp8mm_desc, sms: int, max_smem_bytes: int) -> dict:
+    """The planner's choices for a device with `sms` SMs and `max_smem_bytes`
+    of opt-in shared memory per block, computed on the host without CUDA."""
+    i = fp8mm_plan_info()
+    _check(load().fp8mm_plan_preview(ctypes.byref(desc), int(sms), int(max_smem_bytes), ctypes.byref(i)),
+           "fp8mm_plan_preview")
+    return {k: getattr(i, k) for k, _ in fp8mm_plan_info._fields_}
+

@@ -162,7 +162,12 @@ const char* fp8mm_status_string(fp8mm_status s) {
   return "unknown status";
 }
 
-fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
+// The planner.  With device_checks it reads the SM count and shared-memory
+// limit of desc->device and checks what only the device can answer (the
+// held kernels' register count, resident CTA-pair clusters); without, it
+// plans for the given `sms` and `max_smem` alone (fp8mm_plan_preview).
+static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, bool device_checks,
+                              fp8mm_plan_t** out) {
   if (!desc || !out) return FP8MM_ERR_INVALID;
   *out = nullptr;
   const fp8mm_desc d = *desc;
@@ -190,8 +195,12 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
     ~Guard() { delete p; }
   } guard{P};
   P->d = d;
-  if (cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&P->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device) != cudaSuccess) {
+  if (!device_checks) {
+    P->sms = sms;
+    P->max_smem = max_smem;
+  } else if (cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess ||
+             cudaDeviceGetAttribute(&P->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.device) !=
+                 cudaSuccess) {
     cudaGetLastError();
     return FP8MM_ERR_CUDA;
   }
@@ -300,7 +309,7 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   P->ew = d.epi_warps ? d.epi_warps : ((P->slow && !mx && bn == 128 && P->cg == 1) ? 16 : 8);
   KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
-  if (held_tile(bn, P->slow != 0, mx)) {
+  if (device_checks && held_tile(bn, P->slow != 0, mx)) {
     // The warpgroup register split only redistributes what the block was
     // launched with; refuse the plan if the compiled kernel holds fewer
     // registers per thread than the split hands out (its raise would wait
@@ -387,7 +396,9 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   if (cols > 512) return FP8MM_ERR_UNSUPPORTED;
   P->tmem_cols = cols;
 
-  if (P->cg == 2) {
+  if (P->cg == 2 && !device_checks) {
+    P->grid = 2 * (int)std::min<long long>(P->units, P->sms / 2);  // (one pair per two SMs)
+  } else if (P->cg == 2) {
     // Persistent grid: as many CTA pairs as can be resident at once.
     int nclusters = 0;
     cudaLaunchConfig_t cfg = {};
@@ -417,6 +428,21 @@ fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
   *out = P;
   P = nullptr;  // ownership passes to the caller
   return FP8MM_OK;
+}
+
+fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out) {
+  return plan_impl(desc, 0, 0, true, out);
+}
+
+fp8mm_status fp8mm_plan_preview(const fp8mm_desc* desc, int32_t sms, int32_t max_smem_bytes,
+                                fp8mm_plan_info* info) {
+  if (!info || sms < 2 || max_smem_bytes <= 0) return FP8MM_ERR_INVALID;
+  fp8mm_plan_t* P = nullptr;
+  const fp8mm_status st = plan_impl(desc, sms, max_smem_bytes, false, &P);
+  if (st != FP8MM_OK) return st;
+  const fp8mm_status st2 = fp8mm_plan_get_info(P, info);
+  delete P;
+  return st2;
 }
 
 fp8mm_status fp8mm_workspace_size(const fp8mm_plan_t* plan, size_t* bytes) {

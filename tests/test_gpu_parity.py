@@ -234,3 +234,19 @@ def test_cta_pair_matches_single_cta_within_bound():
     assert pl1.info()["cta_pair"] == 1 and pl2.info()["cta_pair"] == 0
     check(p, c1, a1)
     check(p, c2, a2)
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096, 1, 1), (4096, 4096, 4096, 0, 1), (16, 28672, 8192, 1, 1),
+                                   (8192, 7168, 2048, 0, 2), (4096, 4096, 4096, 1, 3)])
+def test_plan_preview_matches_device_plan(shape):
+    # the host-only preview (used by the CPU planner tests) chooses what the device plan chooses
+    M, N, K, fast, mode = shape
+    L = 4 if mode == 3 else 1
+    d = pm.make_desc(M, N, K, L, out_dtype=0 if mode == 3 else 1, fast_accum=fast, scale_mode=mode)
+    props = torch.cuda.get_device_properties(0)
+    smem = getattr(props, "shared_memory_per_block_optin", 232448)
+    pre = pm._binding.fp8mm_plan_preview(d, props.multi_processor_count, smem)
+    got = pm.Plan(d).info()
+    keys = ("swap_ab", "block_n", "splitk", "stages", "units", "slow", "smem_bytes", "cta_pair", "epi_warps")
+    assert {k: pre[k] for k in keys} == {k: got[k] for k in keys}
+

@@ -1,0 +1,104 @@
+"""The planner's choices, computed on the host without CUDA (fp8mm_plan_preview).
+
+These pin the tile shapes, CTA pairing, split-K, swap-AB, epilogue warps and
+ring depths that the kernels were measured with, for a GB300 (152 SMs,
+227 KiB of opt-in shared memory per block), plus the plan-time refusals.
+A GPU test checks that the preview agrees with fp8mm_plan on the device.
+"""
+import pytest
+
+from precision_matmul_gb300 import _binding as B
+from precision_matmul_gb300 import build as cuda_build
+
+SMS, SMEM = 152, 232448
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()  # nvcc cross-compiles without a GPU; the planner runs on the host
+    return B.load()
+
+
+def preview(M, N, K, L=1, sms=SMS, smem=SMEM, **kw):
+    return B.fp8mm_plan_preview(B.make_desc(M, N, K, L, **kw), sms, smem)
+
+
+def status(M, N, K, L=1, **kw):
+    try:
+        preview(M, N, K, L, **kw)
+        return B.FP8MM_OK
+    except B.FP8MMError as e:
+        return e.status
+
+
+def test_llm_4096_fast_uses_pair_tiles(lib):
+    i = preview(4096, 4096, 4096, out_dtype=1, fast_accum=1)
+    assert (i["cta_pair"], i["block_n"], i["splitk"], i["swap_ab"]) == (1, 224, 1, 0)
+    assert i["units"] == 16 * 19 and i["stages"] == 6 and i["grid"] == SMS
+
+
+def test_llm_4096_slow_uses_held_256_column_tiles(lib):
+    i = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0)
+    assert (i["cta_pair"], i["block_n"], i["splitk"], i["epi_warps"], i["slow"]) == (0, 256, 1, 8, 1)
+    assert i["stages"] == 4
+
+
+@pytest.mark.parametrize("mode,stages", [(B.FP8MM_SCALE_A1x128_B128x128, 3), (B.FP8MM_SCALE_A1x128_B1x128, 2)])
+def test_blockwise_shallow_ring(lib, mode, stages):
+    i = preview(8192, 7168, 2048, out_dtype=1, scale_mode=mode, fast_accum=1)  # block scales are always slow
+    assert (i["block_n"], i["slow"], i["stages"], i["epi_warps"]) == (256, 1, stages, 8)
+
+
+def test_mx_batched_held_256(lib):
+    i = preview(4096, 4096, 4096, 4, scale_mode=B.FP8MM_SCALE_MX32_UE8M0, out_dtype=0, fast_accum=1)
+    assert (i["block_n"], i["cta_pair"], i["splitk"], i["stages"]) == (256, 0, 1, 4)
+    assert i["units"] == 4 * 32 * 16
+
+
+@pytest.mark.parametrize("M,fast,swap,bn,splitk,pair", [
+    (16, 1, 1, 16, 2, 0), (16, 0, 1, 16, 2, 0), (64, 1, 1, 64, 2, 0),
+    (256, 1, 0, 224, 1, 1), (256, 0, 0, 256, 1, 0),
+    (1024, 1, 0, 256, 1, 1), (2048, 1, 0, 256, 1, 1), (8192, 1, 0, 256, 1, 1), (8192, 0, 0, 256, 1, 0),
+])
+def test_skinny_sweep(lib, M, fast, swap, bn, splitk, pair):
+    i = preview(M, 28672, 8192, out_dtype=1, fast_accum=fast)
+    assert (i["swap_ab"], i["block_n"], i["splitk"], i["cta_pair"]) == (swap, bn, splitk, pair)
+
+
+def test_workspace_free_plans_have_no_split(lib):
+    i = preview(256, 256, 256, out_dtype=0, fast_accum=1)
+    assert i["splitk"] == 1 and i["units"] >= 1
+
+
+@pytest.mark.parametrize("kw,st", [
+    (dict(block_n=256, fast_accum=0, splitk=2), B.FP8MM_ERR_UNSUPPORTED),           # held tiles are never split
+    (dict(block_n=192, scale_mode=B.FP8MM_SCALE_MX32_UE8M0), B.FP8MM_ERR_UNSUPPORTED),  # MX widths 128/224/256
+    (dict(block_n=224, scale_mode=B.FP8MM_SCALE_MX32_UE8M0), B.FP8MM_OK),
+    (dict(cta_pair=1, scale_mode=B.FP8MM_SCALE_MX32_UE8M0), B.FP8MM_ERR_UNSUPPORTED),
+    (dict(block_n=256, fast_accum=0, epi_warps=16), B.FP8MM_OK),
+    (dict(block_n=48), B.FP8MM_ERR_UNSUPPORTED),                                    # not instantiated
+    (dict(epi_warps=12), B.FP8MM_ERR_INVALID),
+    (dict(stages=13), B.FP8MM_ERR_INVALID),
+])
+def test_plan_time_refusals(lib, kw, st):
+    base = dict(out_dtype=0, fast_accum=1)
+    base.update(kw)
+    assert status(512, 1024, 1024, **base) == st
+
+
+def test_small_devices_and_shared_memory(lib):
+    i = preview(4096, 4096, 4096, sms=8, out_dtype=1, fast_accum=1)
+    assert i["grid"] <= 8
+    # less shared memory: fewer stages, same tile
+    full = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0)
+    small = preview(4096, 4096, 4096, smem=160 * 1024, out_dtype=1, fast_accum=0)
+    assert small["block_n"] == full["block_n"] and small["stages"] < full["stages"]
+    assert status(4096, 4096, 4096, smem=40 * 1024, out_dtype=1, fast_accum=0) == B.FP8MM_ERR_UNSUPPORTED
+
+
+def test_preview_rejects_bad_device_description(lib):
+    d = B.make_desc(64, 64, 64)
+    for sms, smem in ((0, SMEM), (1, SMEM), (SMS, 0)):
+        with pytest.raises(B.FP8MMError) as e:
+            B.fp8mm_plan_preview(d, sms, smem)
+        assert e.value.status == B.FP8MM_ERR_INVALID
