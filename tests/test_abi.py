@@ -55,6 +55,37 @@ def test_structs_match_the_header_layout(tmp_path):
     assert got == want
 
 
+def test_plain_c_caller_links_and_plans(lib, tmp_path):
+    # a C program against the header alone: link with the library, plan the
+    # 4096^3 slow GEMM for a 152-SM device on the host, print the choices
+    import subprocess
+    src = tmp_path / "caller.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "fp8mm.h"
+int main(void) {
+  fp8mm_desc d;
+  memset(&d, 0, sizeof d);
+  d.M = d.N = d.K = 4096; d.L = 1;
+  d.out_dtype = FP8MM_OUT_BF16; d.fast_accum = 0;
+  fp8mm_plan_info i;
+  fp8mm_status st = fp8mm_plan_preview(&d, 152, 232448, &i);
+  printf("%s %d %d %d %d\n", fp8mm_status_string(st), i.block_n, i.cta_pair, i.splitk, i.slow);
+  d.K = 24;  /* K rows must be 16-byte multiples */
+  printf("%s\n", fp8mm_status_string(fp8mm_plan_preview(&d, 152, 232448, &i)));
+  return st == FP8MM_OK ? 0 : 1;
+}
+""")
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(cuda_build.LIB)
+    subprocess.run(["gcc", "-I" + os.path.join(ROOT, "include"), str(src), "-L" + libdir, "-lfp8mm",
+                    "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert out[0].split()[1:] == ["256", "0", "1", "1"]
+    assert "ALIGN" in out[1].upper()
+
+
 def test_status_strings(lib):
     for code in range(8):
         assert B.fp8mm_status_string(code)
