@@ -18,10 +18,9 @@ Algebra Operators" (GemmFP8FwdOp scale forms); cuDNN "GEMM + Amax (SM100)"
 (Shapes, Equations, the physical scale-factor atom layout).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in
-``tests/test_oracle_*.py`` except the reading of the MX scale-factor row order
-inside one 128-row atom (row = i32 + 32*i4), which is pinned only by
-self-consistency with the page's stated permutation: "parity unpinned" beyond
-that.
+``tests/test_oracle_*.py``.  The reading of the MX scale-factor row order inside
+one 128-row atom (row = i32 + 32*i4) is pinned against torch's own layout
+routine for the same hardware factors.
 """
 from __future__ import annotations
 

@@ -4,8 +4,9 @@ Each check reaches the expected value by a route that shares nothing with the
 oracle's C code: exact rationals (``fractions.Fraction``) on tiny K, torch's
 float64 matmul where the float64 sum is exact, algebraic invariants (power-of-
 two scale linearity, layout equivalence, constant block scales = per-tensor,
-unit MX factors = per-tensor) and the page's own logical-to-physical
-permutation of the MX scale-factor atoms.
+unit MX factors = per-tensor), the page's own logical-to-physical
+permutation of the MX scale-factor atoms and torch's layout routine for the
+same factors.
 """
 from fractions import Fraction
 import math
@@ -273,6 +274,60 @@ def test_mx_factor_layout_through_page_permutation(facts):
     refab = torch.bmm(Ah.abs(), Bh.abs().transpose(1, 2)).numpy()
     assert np.all(np.abs(ce - ref) <= refab * K * 2.0 ** -52)
     assert np.allclose(ab, refab, rtol=1e-12, atol=0)
+
+
+def _library_blocked_layout():
+    """torch's own routine that lays out MX scale factors for its block-scaled
+    matmul (the cuBLAS "D block scaling factors layout": 128-row by 4-factor
+    atoms).  Its module imports test-only packages, so the two functions are
+    compiled from torch's installed source by themselves."""
+    import ast
+    import importlib.util
+    spec = importlib.util.find_spec("torch.testing._internal.common_quantized")
+    if spec is None or spec.origin is None:
+        pytest.skip("torch ships no blocked-layout helper")
+    with open(spec.origin) as f:
+        tree = ast.parse(f.read())
+    fns = [n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name in ("ceil_div", "to_blocked")]
+    if len(fns) != 2:
+        pytest.skip("torch's blocked-layout helper not found")
+    ns = {"torch": torch}
+    exec(compile(ast.Module(body=fns, type_ignores=[]), spec.origin, "exec"), ns)
+    return ns["to_blocked"]
+
+
+def test_mx_factor_layout_matches_the_library_blocked_layout():
+    # The row order inside one 128-row atom (row = i32 + 32*i4) is a reading of
+    # the page's logical modes.  torch lays out the same hardware factors with
+    # an implementation of its own; factors placed by it must give the oracle
+    # the per-element dequantize-then-matmul result.
+    to_blocked = _library_blocked_layout()
+    L, M, N, K = 2, 200, 136, 416  # ragged rows, factor columns padded to a multiple of 4
+    p = synth.mx_batched(L=L, M=M, N=N, K=K, seed=62)
+    a, b = p.a.numpy(), p.b.numpy()
+    g = torch.Generator().manual_seed(63)
+
+    def factors(R):
+        codes = torch.randint(121, 134, (L, R, (K + 31) // 32), generator=g, dtype=torch.int32)
+        phys = torch.cat([to_blocked(codes[l]) for l in range(L)]).to(torch.uint8)
+        per_elem = torch.exp2((codes.double() - 127).repeat_interleave(32, dim=2)[:, :, :K])
+        return phys.numpy(), per_elem
+
+    sfa, ea = factors(M)
+    sfb, eb = factors(N)
+    assert sfa.size == L * ((M + 127) // 128) * ((K + 127) // 128) * 512
+    ce, _, ab = oracle.scaled_gemm(a, b, sfa, sfb, scale_mode=oracle.SCALE_MX32_UE8M0)
+    Ah = torch.as_tensor(a).view(torch.float8_e4m3fn).double() * ea
+    Bh = torch.as_tensor(b).view(torch.float8_e4m3fn).double() * eb
+    ref = torch.bmm(Ah, Bh.transpose(1, 2)).numpy()
+    refab = torch.bmm(Ah.abs(), Bh.abs().transpose(1, 2)).numpy()
+    assert np.all(np.abs(ce - ref) <= refab * K * 2.0 ** -52)
+    # another row order inside the atom (i4 fastest) gives another result
+    MB, KB = (M + 127) // 128, (K + 127) // 128
+    swapped = sfa.reshape(L, MB, KB, 32, 4, 4).transpose(0, 1, 2, 4, 3, 5).copy().reshape(-1)
+    assert not np.array_equal(swapped, sfa)
+    ce_s = oracle.scaled_gemm(a, b, swapped, sfb, scale_mode=oracle.SCALE_MX32_UE8M0)[0]
+    assert not np.all(np.abs(ce_s - ref) <= refab * K * 2.0 ** -52)
 
 
 def test_amax_definition():
