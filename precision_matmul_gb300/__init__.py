@@ -25,7 +25,7 @@ from ._binding import (FP8MM_E4M3, FP8MM_E5M2, FP8MM_OUT_BF16, FP8MM_OUT_F16, FP
                        FP8MM_SCALE_TENSOR, FP8MMError, Plan, fp8mm_device_error, fp8mm_gemm, fp8mm_plan,
                        fp8mm_run, fp8mm_status_string, make_desc)
 
-__all__ = ["scaled_mm", "plan_for", "Plan", "FP8MMError", "fp8mm_plan", "fp8mm_run", "fp8mm_gemm",
+__all__ = ["scaled_mm", "describe", "plan_for", "Plan", "FP8MMError", "fp8mm_plan", "fp8mm_run", "fp8mm_gemm",
            "fp8mm_device_error", "fp8mm_status_string", "make_desc", "FP8MM_E4M3", "FP8MM_E5M2",
            "FP8MM_OUT_F32", "FP8MM_OUT_BF16", "FP8MM_OUT_F16", "FP8MM_SCALE_TENSOR",
            "FP8MM_SCALE_A1x128_B1x128", "FP8MM_SCALE_A1x128_B128x128", "FP8MM_SCALE_MX32_UE8M0"]
@@ -42,13 +42,18 @@ def _torch():
 
 def _fmt_of(t, explicit):
     torch = _torch()
-    if explicit is not None:
-        return int(explicit)
-    if t.dtype == torch.float8_e4m3fn:
-        return FP8MM_E4M3
-    if t.dtype == torch.float8_e5m2:
-        return FP8MM_E5M2
-    raise TypeError(f"operand dtype {t.dtype}: pass float8_e4m3fn / float8_e5m2, or uint8 codes with a_fmt/b_fmt")
+    native = {torch.float8_e4m3fn: FP8MM_E4M3, torch.float8_e5m2: FP8MM_E5M2}.get(t.dtype)
+    if native is None and t.dtype != torch.uint8:
+        raise TypeError(f"operand dtype {t.dtype}: pass float8_e4m3fn / float8_e5m2, or uint8 codes with a_fmt/b_fmt")
+    if explicit is None:
+        if native is None:
+            raise TypeError("uint8 operand codes need their format (a_fmt / b_fmt)")
+        return native
+    if int(explicit) not in (FP8MM_E4M3, FP8MM_E5M2):
+        raise ValueError(f"format {explicit}: FP8MM_E4M3 or FP8MM_E5M2")
+    if native is not None and int(explicit) != native:
+        raise ValueError(f"operand dtype {t.dtype} contradicts format {explicit}")
+    return int(explicit)
 
 
 def _out_code(dtype):
@@ -59,18 +64,85 @@ def _out_code(dtype):
     return table[dtype]
 
 
-def _infer_scale_mode(scale_a, scale_b, L, M, N, K):
+def _mx_dtypes():
     torch = _torch()
-    if scale_a.dtype in (torch.uint8, getattr(torch, "float8_e8m0fnu", torch.uint8)):
+    return (torch.uint8,) + ((torch.float8_e8m0fnu,) if hasattr(torch, "float8_e8m0fnu") else ())
+
+
+def _scale_elems(mode, L, M, N, K):
+    """Elements of (scale_a, scale_b) that the kernels read for a scale form:
+    one fp32 each per tensor; fp32 [L][M][ceil(K/128)] for 1x128 A scales and
+    [L][N][..] / [L][ceil(N/128)][..] for B; one 512-byte UE8M0 atom per 128
+    rows and 128 K for MX factors."""
+    kb = (K + 127) // 128
+    if mode == FP8MM_SCALE_TENSOR:
+        return 1, 1
+    if mode == FP8MM_SCALE_A1x128_B1x128:
+        return L * M * kb, L * N * kb
+    if mode == FP8MM_SCALE_A1x128_B128x128:
+        return L * M * kb, L * ((N + 127) // 128) * kb
+    if mode == FP8MM_SCALE_MX32_UE8M0:
+        return L * ((M + 127) // 128) * kb * 512, L * ((N + 127) // 128) * kb * 512
+    raise ValueError(f"scale_mode {mode}: one of the FP8MM_SCALE_* forms")
+
+
+def _infer_scale_mode(scale_a, scale_b, L, M, N, K):
+    if scale_a.dtype in _mx_dtypes():
         return FP8MM_SCALE_MX32_UE8M0
     if scale_a.numel() == 1 and scale_b.numel() == 1:
         return FP8MM_SCALE_TENSOR
-    kb = (K + 127) // 128
-    if scale_b.numel() == L * N * kb and scale_a.numel() == L * M * kb:
-        return FP8MM_SCALE_A1x128_B1x128
-    if scale_b.numel() == L * ((N + 127) // 128) * kb and scale_a.numel() == L * M * kb:
-        return FP8MM_SCALE_A1x128_B128x128
+    for mode in (FP8MM_SCALE_A1x128_B1x128, FP8MM_SCALE_A1x128_B128x128):
+        if (scale_a.numel(), scale_b.numel()) == _scale_elems(mode, L, M, N, K):
+            return mode
     raise ValueError("cannot infer the scale form from the scale shapes; pass scale_mode")
+
+
+def describe(a, b, scale_a, scale_b, *, out_dtype=None, a_fmt=None, b_fmt=None, scale_mode=None, out=None,
+             amax=None):
+    """Check the arguments of ``scaled_mm`` on the host and return
+    ``(L, M, N, K, a_fmt, b_fmt, scale_mode, out_code, out_shape)``.
+
+    Everything the kernels will read or write is checked here, because the C
+    ABI only sees pointers: operand formats, that every tensor sits on one
+    device and is contiguous, and that the scale tensors hold exactly the
+    elements their form reads (a short scale tensor would be read past its
+    end on the device).  Raises TypeError or ValueError."""
+    torch = _torch()
+    if out_dtype is None:
+        out_dtype = torch.bfloat16
+    batched = a.dim() == 3
+    if a.dim() not in (2, 3) or b.dim() != a.dim():
+        raise ValueError("a and b must both be [M, K] or both [L, M, K]")
+    L = a.shape[0] if batched else 1
+    M, K = a.shape[-2], a.shape[-1]
+    N = b.shape[-2]
+    if b.shape[-1] != K or (batched and b.shape[0] != L):
+        raise ValueError("a and b disagree on K or L")
+    tensors = [a, b, scale_a, scale_b] + [t for t in (out, amax) if t is not None]
+    if any(t.device != a.device for t in tensors):
+        raise ValueError("all tensors must be on one device")
+    if not all(t.is_contiguous() for t in tensors):
+        raise ValueError("a, b, the scales, out and amax must be contiguous (K innermost for a and b)")
+    fa, fb = _fmt_of(a, a_fmt), _fmt_of(b, b_fmt)
+    oc = _out_code(out_dtype)
+    mode = int(scale_mode) if scale_mode is not None else _infer_scale_mode(scale_a, scale_b, L, M, N, K)
+    want_a, want_b = _scale_elems(mode, L, M, N, K)
+    if mode == FP8MM_SCALE_MX32_UE8M0:
+        if scale_a.dtype not in _mx_dtypes() or scale_b.dtype not in _mx_dtypes():
+            raise TypeError("MX factors are uint8 / float8_e8m0fnu UE8M0 codes")
+        if fa != fb:
+            raise ValueError("the MX form needs A and B of one format")
+    elif scale_a.dtype != torch.float32 or scale_b.dtype != torch.float32:
+        raise TypeError("per-tensor and block scales are float32")
+    if (scale_a.numel(), scale_b.numel()) != (want_a, want_b):
+        raise ValueError(f"scale form {mode} reads {want_a} / {want_b} scale elements for A / B; "
+                         f"got {scale_a.numel()} / {scale_b.numel()}")
+    shape = (L, M, N) if batched else (M, N)
+    if out is not None and (tuple(out.shape) != shape or out.dtype != out_dtype):
+        raise ValueError("out has the wrong shape or dtype")
+    if amax is not None and (amax.dtype != torch.float32 or amax.numel() < 1):
+        raise ValueError("amax must hold at least one float32")
+    return L, M, N, K, fa, fb, mode, oc, shape
 
 
 def plan_for(desc_key: tuple) -> Plan:
@@ -118,31 +190,17 @@ def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a
     torch = _torch()
     if out_dtype is None:
         out_dtype = torch.bfloat16
-    batched = a.dim() == 3
-    if a.dim() not in (2, 3) or b.dim() != a.dim():
-        raise ValueError("a and b must both be [M, K] or both [L, M, K]")
-    if not (a.is_cuda and b.is_cuda and scale_a.is_cuda and scale_b.is_cuda):
+    if not a.is_cuda:
         raise ValueError("all inputs must be CUDA tensors")
-    L = a.shape[0] if batched else 1
-    M, K = a.shape[-2], a.shape[-1]
-    N = b.shape[-2]
-    if b.shape[-1] != K or (batched and b.shape[0] != L):
-        raise ValueError("a and b disagree on K or L")
-    if not (a.is_contiguous() and b.is_contiguous() and scale_a.is_contiguous() and scale_b.is_contiguous()):
-        raise ValueError("a, b and the scales must be contiguous (K innermost)")
-    fa, fb = _fmt_of(a, a_fmt), _fmt_of(b, b_fmt)
-    oc = _out_code(out_dtype)
-    mode = scale_mode if scale_mode is not None else _infer_scale_mode(scale_a, scale_b, L, M, N, K)
+    L, M, N, K, fa, fb, mode, oc, shape = describe(a, b, scale_a, scale_b, out_dtype=out_dtype, a_fmt=a_fmt,
+                                                   b_fmt=b_fmt, scale_mode=scale_mode, out=out, amax=amax)
     device = a.device.index if a.device.index is not None else torch.cuda.current_device()
     fast = 1 if use_fast_accum else 0
     key = (M, N, K, L, fa, fb, int(mode), oc, fast, int(splitk), int(swap_ab), int(block_n), device, int(cta_pair),
            int(epi_warps))
     plan = plan_for(key)
-    shape = (L, M, N) if batched else (M, N)
     if out is None:
         out = torch.empty(shape, dtype=out_dtype, device=a.device)
-    elif tuple(out.shape) != shape or out.dtype != out_dtype or not out.is_contiguous():
-        raise ValueError("out has the wrong shape, dtype or layout")
     if amax is None:
         amax = torch.empty(1, dtype=torch.float32, device=a.device)
     stream = torch.cuda.current_stream(a.device).cuda_stream
