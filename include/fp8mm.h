@@ -132,7 +132,8 @@ fp8mm_status fp8mm_workspace_size(const fp8mm_plan_t* plan, size_t* bytes);
 /* Enqueue one GEMM + amax on `stream` (a cudaStream_t; NULL = legacy default
  * stream).  a, b, scale_a, scale_b, c, amax, workspace: device pointers laid
  * out as described above.  a, b and c must be 16-byte aligned; scale pointers
- * 4-byte aligned.  c and amax are written, never read. */
+ * 4-byte aligned (MX factor atoms 16-byte aligned), workspace 256-byte
+ * aligned; else FP8MM_ERR_ALIGNMENT.  c and amax are written, never read. */
 fp8mm_status fp8mm_run(fp8mm_plan_t* plan, const void* a, const void* b, const void* scale_a,
                        const void* scale_b, void* c, float* amax, void* workspace,
                        size_t workspace_bytes, void* stream);
