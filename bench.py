@@ -190,7 +190,7 @@ def oracle_sample(probs, target_s=8.0, max_rows=None):
         rows = 8
         while True:
             t0 = time.perf_counter()
-            oracle.scaled_gemm(a[:1], b[:1], sa if p.scale_mode == 0 else sa, sb, a_fmt=p.a_fmt, b_fmt=p.b_fmt,
+            oracle.scaled_gemm(a[:1], b[:1], sa, sb, a_fmt=p.a_fmt, b_fmt=p.b_fmt,
                                scale_mode=p.scale_mode, out_dtype=p.out_dtype, rows=(0, rows), nthreads=threads)
             dt = time.perf_counter() - t0
             if dt > 0.5 or rows >= p.M:
