@@ -75,7 +75,7 @@ typedef enum {
   FP8MM_ERR_INVALID = 1,     /* null pointer, negative size, value out of range    */
   FP8MM_ERR_ALIGNMENT = 2,   /* a row or pointer is not 16-byte aligned (K % 16, N rows of C) */
   FP8MM_ERR_UNSUPPORTED = 3, /* outside this library: mixed formats in the MX form, sizes >= 2^31 */
-  FP8MM_ERR_REJECTED = 4,    /* reserved for a torch-compatible strict mode       */
+  FP8MM_ERR_REJECTED = 4,    /* a format pair torch._scaled_mm refuses (only with strict_torch) */
   FP8MM_ERR_WORKSPACE = 5,   /* workspace missing or smaller than fp8mm_workspace_size */
   FP8MM_ERR_CUDA = 6,        /* a CUDA runtime call or the launch failed           */
   FP8MM_ERR_DEVICE = 7       /* the kernel aborted (see fp8mm_device_error)        */
@@ -101,6 +101,9 @@ typedef struct {
   int32_t cta_pair;    /* two-SM (CTA pair) tiles: 0 choose; 1 force on; 2 force off */
   int32_t epi_warps;   /* epilogue warps per CTA: 0 choose, 8 or 16 */
   int32_t stages;      /* shared-memory pipeline depth: 0 choose (as many as fit), else 2..12 */
+  int32_t strict_torch; /* 0: accept all four E4M3/E5M2 pairs; 1: refuse with FP8MM_ERR_REJECTED
+                           the pair torch._scaled_mm refuses, E5M2 x E5M2 (mmaemu "Testing
+                           mmaemu", T1 hw_mini, expected error classes) */
 } fp8mm_desc;
 
 typedef struct fp8mm_plan_s fp8mm_plan_t;

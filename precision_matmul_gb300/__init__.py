@@ -145,17 +145,29 @@ def describe(a, b, scale_a, scale_b, *, out_dtype=None, a_fmt=None, b_fmt=None, 
     return L, M, N, K, fa, fb, mode, oc, shape
 
 
+_KEY_LEN = 16
+
+
+def normalize_key(desc_key: tuple) -> tuple:
+    """The canonical plan key: (M, N, K, L, a_fmt, b_fmt, scale_mode, out_dtype,
+    fast_accum, splitk, swap_ab, block_n, device, cta_pair, epi_warps,
+    strict_torch), with fields left off the end taken as 0."""
+    key = tuple(int(x) for x in desc_key)
+    if not 13 <= len(key) <= _KEY_LEN:
+        raise ValueError(f"plan key of {len(key)} fields")
+    return key + (0,) * (_KEY_LEN - len(key))
+
+
 def plan_for(desc_key: tuple) -> Plan:
-    """Cached plan for a description tuple (see ``scaled_mm``)."""
+    """Cached plan for a description tuple (see ``normalize_key``)."""
+    k = normalize_key(desc_key)
     with _lock:
-        p = _plans.get(desc_key)
+        p = _plans.get(k)
         if p is None:
-            p = Plan(make_desc(*desc_key[:4], a_fmt=desc_key[4], b_fmt=desc_key[5], scale_mode=desc_key[6],
-                               out_dtype=desc_key[7], fast_accum=desc_key[8], splitk=desc_key[9],
-                               swap_ab=desc_key[10], block_n=desc_key[11], device=desc_key[12],
-                               cta_pair=desc_key[13] if len(desc_key) > 13 else 0,
-                               epi_warps=desc_key[14] if len(desc_key) > 14 else 0))
-            _plans[desc_key] = p
+            p = Plan(make_desc(*k[:4], a_fmt=k[4], b_fmt=k[5], scale_mode=k[6], out_dtype=k[7], fast_accum=k[8],
+                               splitk=k[9], swap_ab=k[10], block_n=k[11], device=k[12], cta_pair=k[13],
+                               epi_warps=k[14], strict_torch=k[15]))
+            _plans[k] = p
         return p
 
 
@@ -173,7 +185,8 @@ def _workspace(device, stream_handle, nbytes):
 
 
 def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a_fmt=None, b_fmt=None,
-              scale_mode=None, out=None, amax=None, splitk=0, swap_ab=0, block_n=0, cta_pair=0, epi_warps=0):
+              scale_mode=None, out=None, amax=None, splitk=0, swap_ab=0, block_n=0, cta_pair=0, epi_warps=0,
+              strict_torch=False):
     """C = (a * scale_a) @ (b * scale_b)^T and amax = max |C|, on a's CUDA device.
 
     a: [M, K] or [L, M, K]; b: [N, K] or [L, N, K]; both K-contiguous FP8
@@ -183,7 +196,8 @@ def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a
     Returns (C, amax) with C of out_dtype (default bfloat16) and amax a
     one-element fp32 tensor.  splitk, swap_ab, block_n, cta_pair and
     epi_warps override the planner's choices (0 leaves them to it; meanings as
-    in fp8mm_desc).  Enqueued on the current stream; nothing is
+    in fp8mm_desc).  strict_torch=True refuses (FP8MMError, FP8MM_ERR_REJECTED)
+    the format pair torch._scaled_mm refuses, E5M2 x E5M2.  Enqueued on the current stream; nothing is
     synchronised.  One workspace per (device, stream) is reused, so calls on
     one stream must not overlap with calls of another thread on that stream.
     """
@@ -197,7 +211,7 @@ def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a
     device = a.device.index if a.device.index is not None else torch.cuda.current_device()
     fast = 1 if use_fast_accum else 0
     key = (M, N, K, L, fa, fb, int(mode), oc, fast, int(splitk), int(swap_ab), int(block_n), device, int(cta_pair),
-           int(epi_warps))
+           int(epi_warps), int(bool(strict_torch)))
     plan = plan_for(key)
     if out is None:
         out = torch.empty(shape, dtype=out_dtype, device=a.device)

@@ -33,7 +33,8 @@ class fp8mm_desc(ctypes.Structure):
                 ("a_fmt", ctypes.c_int32), ("b_fmt", ctypes.c_int32), ("scale_mode", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("fast_accum", ctypes.c_int32), ("splitk", ctypes.c_int32),
                 ("swap_ab", ctypes.c_int32), ("block_n", ctypes.c_int32), ("device", ctypes.c_int32),
-                ("cta_pair", ctypes.c_int32), ("epi_warps", ctypes.c_int32), ("stages", ctypes.c_int32)]
+                ("cta_pair", ctypes.c_int32), ("epi_warps", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("strict_torch", ctypes.c_int32)]
 
 
 class fp8mm_plan_info(ctypes.Structure):
@@ -101,7 +102,7 @@ def _check(st: int, where: str):
 
 def make_desc(M, N, K, L=1, *, a_fmt=FP8MM_E4M3, b_fmt=FP8MM_E4M3, scale_mode=FP8MM_SCALE_TENSOR,
               out_dtype=FP8MM_OUT_BF16, fast_accum=1, splitk=0, swap_ab=0, block_n=0, device=0,
-              cta_pair=0, epi_warps=0, stages=0) -> fp8mm_desc:
+              cta_pair=0, epi_warps=0, stages=0, strict_torch=0) -> fp8mm_desc:
     d = fp8mm_desc()
     d.M, d.N, d.K, d.L = int(M), int(N), int(K), int(L)
     d.a_fmt, d.b_fmt, d.scale_mode, d.out_dtype = int(a_fmt), int(b_fmt), int(scale_mode), int(out_dtype)
@@ -110,6 +111,7 @@ def make_desc(M, N, K, L=1, *, a_fmt=FP8MM_E4M3, b_fmt=FP8MM_E4M3, scale_mode=FP
     d.cta_pair = int(cta_pair)
     d.epi_warps = int(epi_warps)
     d.stages = int(stages)
+    d.strict_torch = int(strict_torch)
     return d
 
 

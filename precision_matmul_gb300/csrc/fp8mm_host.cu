@@ -180,6 +180,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   if (d.cta_pair < 0 || d.cta_pair > 2) return FP8MM_ERR_INVALID;
   if (d.epi_warps != 0 && d.epi_warps != 8 && d.epi_warps != 16) return FP8MM_ERR_INVALID;
   if (d.stages < 0 || d.stages == 1 || d.stages > 12) return FP8MM_ERR_INVALID;
+  if (d.strict_torch < 0 || d.strict_torch > 1) return FP8MM_ERR_INVALID;
   if (d.block_n != 0 && !(d.block_n >= 16 && d.block_n <= 256 && d.block_n % 16 == 0)) return FP8MM_ERR_INVALID;
   const int64_t lim = (int64_t)1 << 31;
   if (d.M >= lim || d.N >= lim || d.K >= lim || d.L >= 65536) return FP8MM_ERR_UNSUPPORTED;
@@ -187,6 +188,9 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   if ((d.N * out_size(d.out_dtype)) % 16 != 0) return FP8MM_ERR_ALIGNMENT;
   const bool mx = d.scale_mode == FP8MM_SCALE_MX32_UE8M0;
   if (mx && d.a_fmt != d.b_fmt) return FP8MM_ERR_UNSUPPORTED;
+  // torch._scaled_mm refuses E5M2 x E5M2; the library computes it unless the
+  // caller asks for torch's refusals.
+  if (d.strict_torch && d.a_fmt == FP8MM_E5M2 && d.b_fmt == FP8MM_E5M2) return FP8MM_ERR_REJECTED;
 
   fp8mm_plan_s* P = new (std::nothrow) fp8mm_plan_s();
   if (!P) return FP8MM_ERR_INVALID;

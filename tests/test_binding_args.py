@@ -127,3 +127,35 @@ def test_scaled_mm_refuses_host_tensors():
     p = synth.llm_per_tensor(M=32, N=48, K=128)
     with pytest.raises(ValueError):
         pm.scaled_mm(p.a[0], p.b[0], p.scale_a, p.scale_b, a_fmt=0, b_fmt=0)
+
+
+def test_plan_keys_of_every_length_agree():
+    full = (64, 64, 128, 1, 0, 0, 0, 1, 1, 0, 0, 0, 0, 0, 0, 0)
+    assert pm.normalize_key(full[:13]) == full      # without pair, epilogue warps or strictness
+    assert pm.normalize_key(full[:14]) == full
+    assert pm.normalize_key(full[:15]) == full
+    assert pm.normalize_key(full) == full
+    with pytest.raises(ValueError):
+        pm.normalize_key(full[:12])
+    with pytest.raises(ValueError):
+        pm.normalize_key(full + (0,))
+
+
+def test_plan_for_builds_one_descriptor_per_key(monkeypatch):
+    made = []
+
+    class FakePlan:
+        def __init__(self, desc):
+            made.append(desc)
+
+    monkeypatch.setattr(pm, "Plan", FakePlan)
+    monkeypatch.setattr(pm, "_plans", {})
+    p1 = pm.plan_for((64, 80, 128, 2, 1, 0, 0, 2, 1, 3, 2, 64, 0, 2))
+    p2 = pm.plan_for((64, 80, 128, 2, 1, 0, 0, 2, 1, 3, 2, 64, 0, 2, 0, 0))
+    p3 = pm.plan_for((64, 80, 128, 2, 1, 0, 0, 2, 1, 3, 2, 64, 0, 2, 16, 1))
+    assert p1 is p2 and p3 is not p1 and len(made) == 2
+    d, e = made
+    assert (d.M, d.N, d.K, d.L, d.a_fmt, d.b_fmt, d.scale_mode, d.out_dtype, d.fast_accum) == (64, 80, 128, 2, 1, 0, 0, 2, 1)
+    assert (d.splitk, d.swap_ab, d.block_n, d.device, d.cta_pair, d.epi_warps, d.stages, d.strict_torch) == \
+        (3, 2, 64, 0, 2, 0, 0, 0)
+    assert (e.epi_warps, e.strict_torch) == (16, 1)

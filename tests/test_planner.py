@@ -102,3 +102,22 @@ def test_preview_rejects_bad_device_description(lib):
         with pytest.raises(B.FP8MMError) as e:
             B.fp8mm_plan_preview(d, sms, smem)
         assert e.value.status == B.FP8MM_ERR_INVALID
+
+
+@pytest.mark.parametrize("fa,fb,mode,st", [
+    (1, 1, B.FP8MM_SCALE_TENSOR, B.FP8MM_ERR_REJECTED),          # torch._scaled_mm refuses E5M2 x E5M2
+    (1, 1, B.FP8MM_SCALE_A1x128_B128x128, B.FP8MM_ERR_REJECTED),
+    (1, 1, B.FP8MM_SCALE_MX32_UE8M0, B.FP8MM_ERR_REJECTED),
+    (0, 1, B.FP8MM_SCALE_TENSOR, B.FP8MM_OK),
+    (1, 0, B.FP8MM_SCALE_TENSOR, B.FP8MM_OK),
+    (0, 0, B.FP8MM_SCALE_TENSOR, B.FP8MM_OK),
+])
+def test_strict_torch_refuses_what_torch_refuses(lib, fa, fb, mode, st):
+    kw = dict(a_fmt=fa, b_fmt=fb, scale_mode=mode, out_dtype=0, fast_accum=1)
+    assert status(512, 1024, 1024, strict_torch=1, **kw) == st
+    assert status(512, 1024, 1024, **kw) == B.FP8MM_OK                # the library's own default computes all four
+
+
+def test_strict_torch_flag_values(lib):
+    assert status(512, 1024, 1024, out_dtype=0, strict_torch=2) == B.FP8MM_ERR_INVALID
+    assert status(512, 1024, 1024, out_dtype=0, strict_torch=-1) == B.FP8MM_ERR_INVALID
