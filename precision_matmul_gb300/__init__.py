@@ -25,7 +25,7 @@ from ._binding import (FP8MM_E4M3, FP8MM_E5M2, FP8MM_OUT_BF16, FP8MM_OUT_F16, FP
                        FP8MM_SCALE_TENSOR, FP8MMError, Plan, fp8mm_device_error, fp8mm_gemm, fp8mm_plan,
                        fp8mm_run, fp8mm_status_string, make_desc)
 
-__all__ = ["scaled_mm", "describe", "plan_for", "Plan", "FP8MMError", "fp8mm_plan", "fp8mm_run", "fp8mm_gemm",
+__all__ = ["scaled_mm", "torch_scaled_mm", "describe", "plan_for", "Plan", "FP8MMError", "fp8mm_plan", "fp8mm_run", "fp8mm_gemm",
            "fp8mm_device_error", "fp8mm_status_string", "make_desc", "FP8MM_E4M3", "FP8MM_E5M2",
            "FP8MM_OUT_F32", "FP8MM_OUT_BF16", "FP8MM_OUT_F16", "FP8MM_SCALE_TENSOR",
            "FP8MM_SCALE_A1x128_B1x128", "FP8MM_SCALE_A1x128_B128x128", "FP8MM_SCALE_MX32_UE8M0"]
@@ -223,3 +223,40 @@ def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a
     plan.run(a.data_ptr(), b.data_ptr(), scale_a.data_ptr(), scale_b.data_ptr(), out.data_ptr(),
              amax.data_ptr(), ws.data_ptr() if ws is not None else None, nbytes, stream)
     return out, amax
+
+
+def torch_scaled_mm(input, mat2, scale_a, scale_b, bias=None, scale_result=None, out_dtype=None,
+                    use_fast_accum=False, *, out=None):
+    """The same GEMM in torch._scaled_mm's calling convention (mmaemu "API
+    reference (v0.1)", mmaemu.scaled_mm, argument table).
+
+    input [M, K] row-major FP8; mat2 [K, N] FP8 in column-major storage (the
+    ``w.t()`` of a row-major [N, K] weight); scale_a, scale_b one-element fp32
+    tensors that multiply the result; out_dtype defaults to input's dtype.
+    Returns the [M, N] result (use ``scaled_mm`` for the fused amax as well).
+
+    As in torch, E5M2 x E5M2 is refused (FP8MMError with FP8MM_ERR_REJECTED).
+    Outside this library, raising NotImplementedError: a bias, FP8 outputs
+    (scale_result is read only for those, so it is ignored otherwise), and
+    row-wise scales.  mat2 in row-major storage raises ValueError: the kernels
+    read both operands K-contiguous.
+    """
+    torch = _torch()
+    if bias is not None:
+        raise NotImplementedError("bias is not supported")
+    if out_dtype is None:
+        out_dtype = input.dtype
+    if out_dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        raise NotImplementedError("FP8 outputs are not supported; pass out_dtype float32, bfloat16 or float16")
+    if input.dim() != 2 or mat2.dim() != 2:
+        raise ValueError("input must be [M, K] and mat2 [K, N]")
+    if mat2.shape[0] != input.shape[1]:
+        raise ValueError("input and mat2 disagree on K")
+    if scale_a.numel() != 1 or scale_b.numel() != 1:
+        raise NotImplementedError("only tensor-wise (one-element) scales")
+    b = mat2.t()  # [N, K]
+    if not b.is_contiguous():
+        raise ValueError("mat2 must be column-major ([K, N] with K contiguous, e.g. w.t() of a row-major weight)")
+    c, _ = scaled_mm(input, b, scale_a, scale_b, out_dtype=out_dtype, use_fast_accum=use_fast_accum,
+                     scale_mode=FP8MM_SCALE_TENSOR, out=out, strict_torch=True)
+    return c

@@ -1,0 +1,74 @@
+"""The torch._scaled_mm calling convention on the host (CPU only).
+
+``torch_scaled_mm`` only rearranges arguments for ``scaled_mm``: mat2 [K, N]
+column-major becomes the [N, K] K-contiguous operand (same storage), the
+scales are tensor-wise, and torch's refusal of E5M2 x E5M2 is requested from
+the planner.  The device call is replaced here by a recorder.
+"""
+import pytest
+import torch
+
+import precision_matmul_gb300 as pm
+
+
+@pytest.fixture
+def calls(monkeypatch):
+    seen = []
+
+    def fake(a, b, sa, sb, **kw):
+        seen.append((a, b, sa, sb, kw))
+        return "C", "amax"
+
+    monkeypatch.setattr(pm, "scaled_mm", fake)
+    return seen
+
+
+def _operands(M=32, N=48, K=64, fa=torch.float8_e4m3fn, fb=torch.float8_e4m3fn):
+    g = torch.Generator().manual_seed(7)
+    a = torch.randn(M, K, generator=g).to(fa)
+    w = torch.randn(N, K, generator=g).to(fb)
+    s = torch.tensor([0.5])
+    return a, w, s, s.clone()
+
+
+def test_column_major_mat2_becomes_the_k_contiguous_operand(calls):
+    a, w, sa, sb = _operands()
+    out = torch.empty(32, 48, dtype=torch.bfloat16)
+    assert pm.torch_scaled_mm(a, w.t(), sa, sb, out_dtype=torch.bfloat16, use_fast_accum=True, out=out) == "C"
+    (a2, b2, sa2, sb2, kw), = calls
+    assert a2 is a and b2.shape == (48, 64) and b2.is_contiguous() and b2.data_ptr() == w.data_ptr()
+    assert sa2 is sa and sb2 is sb
+    assert kw == dict(out_dtype=torch.bfloat16, use_fast_accum=True, scale_mode=pm.FP8MM_SCALE_TENSOR, out=out,
+                      strict_torch=True)
+
+
+def test_defaults_follow_torch(calls):
+    a, w, sa, sb = _operands()
+    with pytest.raises(NotImplementedError):           # out_dtype defaults to input's FP8 dtype
+        pm.torch_scaled_mm(a, w.t(), sa, sb)
+    pm.torch_scaled_mm(a, w.t(), sa, sb, None, torch.tensor([2.0]), torch.float32)  # positional; scale_result ignored
+    kw = calls[-1][4]
+    assert kw["use_fast_accum"] is False and kw["out_dtype"] == torch.float32
+
+
+def test_refusals(calls):
+    a, w, sa, sb = _operands()
+    with pytest.raises(NotImplementedError):
+        pm.torch_scaled_mm(a, w.t(), sa, sb, bias=torch.zeros(48), out_dtype=torch.bfloat16)
+    with pytest.raises(NotImplementedError):
+        pm.torch_scaled_mm(a, w.t(), sa, sb, out_dtype=torch.float8_e5m2)
+    with pytest.raises(NotImplementedError):
+        pm.torch_scaled_mm(a, w.t(), torch.ones(32, 1), torch.ones(1, 48), out_dtype=torch.bfloat16)
+    with pytest.raises(ValueError):                    # row-major [K, N]
+        pm.torch_scaled_mm(a, w.t().contiguous(), sa, sb, out_dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pm.torch_scaled_mm(a, w[:, :32].t(), sa, sb, out_dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pm.torch_scaled_mm(a[None], w.t(), sa, sb, out_dtype=torch.bfloat16)
+    assert not calls
+
+
+def test_e5m2_pair_is_sent_with_torchs_refusal(calls):
+    a, w, sa, sb = _operands(fa=torch.float8_e5m2, fb=torch.float8_e5m2)
+    pm.torch_scaled_mm(a, w.t(), sa, sb, out_dtype=torch.bfloat16)
+    assert calls[-1][4]["strict_torch"] is True
