@@ -32,7 +32,7 @@ import threading
 import numpy as np
 
 FMT_E4M3, FMT_E5M2 = 0, 1
-OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
+OUT_F32, OUT_BF16, OUT_F16, OUT_E4M3, OUT_E5M2 = 0, 1, 2, 3, 4
 SCALE_TENSOR, SCALE_A1x128_B1x128, SCALE_A1x128_B128x128, SCALE_MX32_UE8M0 = 0, 1, 2, 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -87,7 +87,7 @@ def _load():
                                            vp, i64, i64, i64, i32,
                                            vp, i64, i64, i64, i32,
                                            i32, vp, vp, i32,
-                                           vp, vp, vp, i64, i64, i32]
+                                           d, vp, vp, vp, i64, i64, i32]
         lib.oracle_scaled_gemm.restype = i32
         lib.oracle_amax.argtypes = [vp, i64]
         lib.oracle_amax.restype = d
@@ -119,7 +119,8 @@ def encode_sat(fmt: int, values) -> np.ndarray:
 
 
 def round_out(out_dtype: int, values) -> np.ndarray:
-    """Round float64 values once, to nearest even, onto fp32/bf16/fp16."""
+    """Round float64 values once, to nearest even, onto fp32/bf16/fp16 (Inf
+    past the largest finite value) or onto E4M3/E5M2 (saturating)."""
     lib = _load()
     values = np.asarray(values, dtype=np.float64)
     return np.array([lib.oracle_round_out(out_dtype, float(v)) for v in values.ravel()],
@@ -132,8 +133,8 @@ def _ptr(a: np.ndarray | None):
 
 def scaled_gemm(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.ndarray, *,
                 a_fmt: int = FMT_E4M3, b_fmt: int = FMT_E4M3, scale_mode: int = SCALE_TENSOR,
-                out_dtype: int = OUT_F32, rows: tuple[int, int] | None = None,
-                nthreads: int | None = None):
+                out_dtype: int = OUT_F32, scale_result: float | None = None,
+                rows: tuple[int, int] | None = None, nthreads: int | None = None):
     """Evaluate the definition on uint8 code arrays.
 
     A is [L][M][K] (or [M][K]) and B is [L][N][K] (or [N][K]) uint8 arrays of any
@@ -144,6 +145,9 @@ def scaled_gemm(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.n
     Returns ``(C_exact, C_out, absum)``, float64 arrays of shape [L][rows][N]
     (batch dim dropped when the inputs had none): the unrounded value, the value
     rounded once to ``out_dtype``, and sum_k |a_hat b_hat| for the error bound.
+    For the FP8 outputs (OUT_E4M3, OUT_E5M2) ``C_out`` is the FP8 value of
+    ``scale_result * C_exact`` (scale_result, an fp32 number, defaults to 1);
+    for the others scale_result is ignored.
     """
     lib = _load()
     squeeze = A.ndim == 2
@@ -168,10 +172,11 @@ def scaled_gemm(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.n
     absum = np.empty(shape, np.float64)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
+    sr = 1.0 if scale_result is None else float(np.float32(scale_result))
     rc = lib.oracle_scaled_gemm(L, M, N, K,
                                 _ptr(A), A.strides[0], A.strides[1], A.strides[2], a_fmt,
                                 _ptr(B), B.strides[0], B.strides[1], B.strides[2], b_fmt,
-                                scale_mode, _ptr(sa), _ptr(sb), out_dtype,
+                                scale_mode, _ptr(sa), _ptr(sb), out_dtype, sr,
                                 _ptr(C_exact), _ptr(C_out), _ptr(absum), m0, m1, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_scaled_gemm rejected its arguments")
@@ -185,3 +190,10 @@ def amax(C: np.ndarray) -> float:
     lib = _load()
     C = np.ascontiguousarray(C, dtype=np.float64)
     return lib.oracle_amax(_ptr(C), C.size)
+
+
+def amax_before_quantization(C_exact: np.ndarray) -> float:
+    """Amax for an FP8 output: max |C| of the result before scale_result and
+    the FP8 rounding, as an fp32 number (reading: the amax that sets the next
+    quantisation scale is taken on the unquantised result)."""
+    return float(round_out(OUT_F32, [amax(C_exact)])[0])

@@ -31,7 +31,8 @@
  * notes): E4M3 is float8_e4m3fn (no infinities, S.1111.111 is NaN, largest
  * finite 448); E5M2 follows IEEE rules (exponent 31: mantissa 0 is Inf,
  * otherwise NaN); UE8M0 code e means 2^(e-127) and 0xFF is NaN; non-finite
- * values propagate by IEEE arithmetic; bf16/fp16/fp32 outputs overflow to Inf.
+ * values propagate by IEEE arithmetic; bf16/fp16/fp32 outputs overflow to Inf;
+ * FP8 outputs are the result times scale_result, rounded once and saturated.
  *
  * Parity pins (tests/test_oracle_*.py): decode tables against torch's float8
  * casts; brute-force exact rationals on tiny K; power-of-two scale linearity;
@@ -51,6 +52,8 @@
 #define OR_OUT_F32 0
 #define OR_OUT_BF16 1
 #define OR_OUT_F16 2
+#define OR_OUT_E4M3 3
+#define OR_OUT_E5M2 4
 
 #define OR_SCALE_TENSOR 0
 #define OR_SCALE_A1x128_B1x128 1
@@ -132,10 +135,19 @@ double oracle_round_f32(double x) { return round_binary(x, 24, -126, 127); }
 double oracle_round_bf16(double x) { return round_binary(x, 8, -126, 127); }
 double oracle_round_f16(double x) { return round_binary(x, 11, -14, 15); }
 
+uint8_t oracle_encode_e4m3_sat(double x);
+uint8_t oracle_encode_e5m2_sat(double x);
+
+/* FP8 outputs (mmaemu "API reference (v0.1)", mmaemu.scaled_mm: out_dtype
+ * may be float8_e4m3fn or float8_e5m2).  Reading: one rounding to nearest
+ * even on the FP8 grid, saturated to the largest finite value (Inf too); NaN
+ * stays NaN. */
 double oracle_round_out(int out_dtype, double x) {
   switch (out_dtype) {
     case OR_OUT_BF16: return oracle_round_bf16(x);
     case OR_OUT_F16: return oracle_round_f16(x);
+    case OR_OUT_E4M3: return oracle_decode_e4m3(oracle_encode_e4m3_sat(x));
+    case OR_OUT_E5M2: return oracle_decode_e5m2(oracle_encode_e5m2_sat(x));
     default: return oracle_round_f32(x);
   }
 }
@@ -185,6 +197,7 @@ typedef struct {
   int scale_mode;
   const void *scale_a, *scale_b;
   int out_dtype;
+  double scale_result;             /* multiplies the result before an FP8 output's rounding */
   double *C_exact, *C_out, *absum; /* [L][M][N], any may be NULL */
   int64_t m0, m1;                  /* rows [m0, m1) are computed; C arrays hold m1-m0 rows */
   double dec_a[256], dec_b[256];
@@ -288,7 +301,12 @@ static void *run_slice(void *arg) {
       int64_t idx = r * j->N + n;
       if (j->C_exact) j->C_exact[idx] = e;
       if (j->absum) j->absum[idx] = s;
-      if (j->C_out) j->C_out[idx] = oracle_round_out(j->out_dtype, e);
+      if (j->C_out) {
+        /* scale_result is "used only for FP8 outputs" (mmaemu.scaled_mm): the
+         * result is multiplied by it, then rounded once. */
+        const int fp8_out = j->out_dtype == OR_OUT_E4M3 || j->out_dtype == OR_OUT_E5M2;
+        j->C_out[idx] = oracle_round_out(j->out_dtype, fp8_out ? e * j->scale_result : e);
+      }
     }
   }
   return NULL;
@@ -300,10 +318,11 @@ int oracle_scaled_gemm(int64_t L, int64_t M, int64_t N, int64_t K,
                        const uint8_t *A, int64_t sAl, int64_t sAm, int64_t sAk, int a_fmt,
                        const uint8_t *B, int64_t sBl, int64_t sBn, int64_t sBk, int b_fmt,
                        int scale_mode, const void *scale_a, const void *scale_b, int out_dtype,
-                       double *C_exact, double *C_out, double *absum,
+                       double scale_result, double *C_exact, double *C_out, double *absum,
                        int64_t m0, int64_t m1, int nthreads) {
   if (L < 0 || M < 0 || N < 0 || K < 0 || m0 < 0 || m1 > M || m0 > m1) return -1;
   if (scale_mode < 0 || scale_mode > 3) return -1;
+  if (out_dtype < 0 || out_dtype > 4) return -1;
   job_t *j = (job_t *)calloc(1, sizeof(job_t));
   if (!j) return -1;
   j->L = L; j->M = M; j->N = N; j->K = K;
@@ -311,6 +330,7 @@ int oracle_scaled_gemm(int64_t L, int64_t M, int64_t N, int64_t K,
   j->B = B; j->sBl = sBl; j->sBn = sBn; j->sBk = sBk; j->b_fmt = b_fmt;
   j->scale_mode = scale_mode; j->scale_a = scale_a; j->scale_b = scale_b;
   j->out_dtype = out_dtype;
+  j->scale_result = scale_result;
   j->C_exact = C_exact; j->C_out = C_out; j->absum = absum;
   j->m0 = m0; j->m1 = m1;
   for (int c = 0; c < 256; ++c) {
