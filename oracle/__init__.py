@@ -87,7 +87,7 @@ def _load():
                                            vp, i64, i64, i64, i32,
                                            vp, i64, i64, i64, i32,
                                            i32, vp, vp, i32,
-                                           d, vp, vp, vp, i64, i64, i32]
+                                           d, vp, vp, vp, vp, i64, i64, i32]
         lib.oracle_scaled_gemm.restype = i32
         lib.oracle_amax.argtypes = [vp, i64]
         lib.oracle_amax.restype = d
@@ -134,6 +134,7 @@ def _ptr(a: np.ndarray | None):
 def scaled_gemm(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.ndarray, *,
                 a_fmt: int = FMT_E4M3, b_fmt: int = FMT_E4M3, scale_mode: int = SCALE_TENSOR,
                 out_dtype: int = OUT_F32, scale_result: float | None = None,
+                bias: np.ndarray | None = None,
                 rows: tuple[int, int] | None = None, nthreads: int | None = None):
     """Evaluate the definition on uint8 code arrays.
 
@@ -147,7 +148,9 @@ def scaled_gemm(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.n
     rounded once to ``out_dtype``, and sum_k |a_hat b_hat| for the error bound.
     For the FP8 outputs (OUT_E4M3, OUT_E5M2) ``C_out`` is the FP8 value of
     ``scale_result * C_exact`` (scale_result, an fp32 number, defaults to 1);
-    for the others scale_result is ignored.
+    for the others scale_result is ignored.  ``bias`` ([N] values of the
+    output type, as float64) is added to every row before the rounding and is
+    included in ``C_exact`` (not defined for FP8 outputs).
     """
     lib = _load()
     squeeze = A.ndim == 2
@@ -173,10 +176,15 @@ def scaled_gemm(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.n
     if nthreads is None:
         nthreads = os.cpu_count() or 1
     sr = 1.0 if scale_result is None else float(np.float32(scale_result))
+    bias_arr = None
+    if bias is not None:
+        bias_arr = np.ascontiguousarray(bias, dtype=np.float64).reshape(-1)
+        if bias_arr.size != N:
+            raise ValueError("bias must hold N values")
     rc = lib.oracle_scaled_gemm(L, M, N, K,
                                 _ptr(A), A.strides[0], A.strides[1], A.strides[2], a_fmt,
                                 _ptr(B), B.strides[0], B.strides[1], B.strides[2], b_fmt,
-                                scale_mode, _ptr(sa), _ptr(sb), out_dtype, sr,
+                                scale_mode, _ptr(sa), _ptr(sb), out_dtype, sr, _ptr(bias_arr),
                                 _ptr(C_exact), _ptr(C_out), _ptr(absum), m0, m1, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_scaled_gemm rejected its arguments")

@@ -198,6 +198,7 @@ typedef struct {
   const void *scale_a, *scale_b;
   int out_dtype;
   double scale_result;             /* multiplies the result before an FP8 output's rounding */
+  const double *bias;              /* [N] values added to every row, or NULL */
   double *C_exact, *C_out, *absum; /* [L][M][N], any may be NULL */
   int64_t m0, m1;                  /* rows [m0, m1) are computed; C arrays hold m1-m0 rows */
   double dec_a[256], dec_b[256];
@@ -298,6 +299,10 @@ static void *run_slice(void *arg) {
     for (int64_t n = 0; n < j->N; ++n) {
       double e, s;
       one_element(j, l, m, n, &e, &s);
+      /* d = (a s_a) @ (b s_b)^T + bias, bias [N] (TileOPs "Linear Algebra
+       * Operators", GemmFP8FwdOp): added to the exact value, before the one
+       * rounding. */
+      if (j->bias) e += j->bias[n];
       int64_t idx = r * j->N + n;
       if (j->C_exact) j->C_exact[idx] = e;
       if (j->absum) j->absum[idx] = s;
@@ -318,11 +323,13 @@ int oracle_scaled_gemm(int64_t L, int64_t M, int64_t N, int64_t K,
                        const uint8_t *A, int64_t sAl, int64_t sAm, int64_t sAk, int a_fmt,
                        const uint8_t *B, int64_t sBl, int64_t sBn, int64_t sBk, int b_fmt,
                        int scale_mode, const void *scale_a, const void *scale_b, int out_dtype,
-                       double scale_result, double *C_exact, double *C_out, double *absum,
+                       double scale_result, const double *bias,
+                       double *C_exact, double *C_out, double *absum,
                        int64_t m0, int64_t m1, int nthreads) {
   if (L < 0 || M < 0 || N < 0 || K < 0 || m0 < 0 || m1 > M || m0 > m1) return -1;
   if (scale_mode < 0 || scale_mode > 3) return -1;
   if (out_dtype < 0 || out_dtype > 4) return -1;
+  if (bias && (out_dtype == OR_OUT_E4M3 || out_dtype == OR_OUT_E5M2)) return -1; /* not defined by the pages */
   job_t *j = (job_t *)calloc(1, sizeof(job_t));
   if (!j) return -1;
   j->L = L; j->M = M; j->N = N; j->K = K;
@@ -331,6 +338,7 @@ int oracle_scaled_gemm(int64_t L, int64_t M, int64_t N, int64_t K,
   j->scale_mode = scale_mode; j->scale_a = scale_a; j->scale_b = scale_b;
   j->out_dtype = out_dtype;
   j->scale_result = scale_result;
+  j->bias = bias;
   j->C_exact = C_exact; j->C_out = C_out; j->absum = absum;
   j->m0 = m0; j->m1 = m1;
   for (int c = 0; c < 256; ++c) {
