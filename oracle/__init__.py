@@ -31,9 +31,9 @@ import threading
 
 import numpy as np
 
-FMT_E4M3, FMT_E5M2 = 0, 1
+FMT_E4M3, FMT_E5M2, FMT_E2M1 = 0, 1, 2
 OUT_F32, OUT_BF16, OUT_F16, OUT_E4M3, OUT_E5M2 = 0, 1, 2, 3, 4
-SCALE_TENSOR, SCALE_A1x128_B1x128, SCALE_A1x128_B128x128, SCALE_MX32_UE8M0 = 0, 1, 2, 3
+SCALE_TENSOR, SCALE_A1x128_B1x128, SCALE_A1x128_B128x128, SCALE_MX32_UE8M0, SCALE_NV16_E4M3 = 0, 1, 2, 3, 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp8_oracle.c")
@@ -69,7 +69,7 @@ def _load():
         lib = ctypes.CDLL(build())
         d, u8, i64, i32, vp = (ctypes.c_double, ctypes.c_uint8, ctypes.c_int64, ctypes.c_int,
                               ctypes.c_void_p)
-        for name in ("oracle_decode_e4m3", "oracle_decode_e5m2", "oracle_decode_ue8m0"):
+        for name in ("oracle_decode_e4m3", "oracle_decode_e5m2", "oracle_decode_e2m1", "oracle_decode_ue8m0"):
             getattr(lib, name).argtypes = [u8]
             getattr(lib, name).restype = d
         lib.oracle_decode.argtypes = [i32, u8]
@@ -96,9 +96,10 @@ def _load():
 
 
 def decode(fmt: int, codes) -> np.ndarray:
-    """float64 values of FP8 codes (E4M3 or E5M2), decoded bit by bit."""
+    """float64 values of FP8 codes (E4M3 or E5M2) or of FP4 codes (E2M1, one
+    per byte in the low four bits), decoded bit by bit."""
     lib = _load()
-    fn = lib.oracle_decode_e5m2 if fmt == FMT_E5M2 else lib.oracle_decode_e4m3
+    fn = {FMT_E5M2: lib.oracle_decode_e5m2, FMT_E2M1: lib.oracle_decode_e2m1}.get(fmt, lib.oracle_decode_e4m3)
     codes = np.asarray(codes, dtype=np.uint8)
     return np.array([fn(int(c)) for c in codes.ravel()], dtype=np.float64).reshape(codes.shape)
 
@@ -127,6 +128,17 @@ def round_out(out_dtype: int, values) -> np.ndarray:
                     dtype=np.float64).reshape(values.shape)
 
 
+def unpack_fp4(packed: np.ndarray) -> np.ndarray:
+    """One E2M1 code per byte from packed FP4 operands (float4_e2m1fn_x2: two
+    values per byte along the contiguous dimension).  Reading: element 2i sits
+    in the low four bits of byte i and element 2i + 1 in the high four bits."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(packed.shape[:-1] + (2 * packed.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = packed & 0x0F
+    out[..., 1::2] = packed >> 4
+    return out
+
+
 def _ptr(a: np.ndarray | None):
     return None if a is None else ctypes.c_void_p(a.ctypes.data)
 
@@ -143,6 +155,11 @@ def scaled_gemm(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.n
     layout-equivalence pin feeds NN/TN/TT operands).  Scales: float32 arrays for
     the per-tensor and block modes, uint8 UE8M0 atoms for the MX mode.
 
+    FP4 operands (``a_fmt = b_fmt = FMT_E2M1``) are given packed, [L][M][K/2]
+    and [L][N][K/2] bytes (``unpack_fp4``); they go with the block-scaled forms
+    SCALE_MX32_UE8M0 (UE8M0 per 32 along K) or SCALE_NV16_E4M3 (E4M3 factor
+    codes per 16 along K), both in the atom layout.
+
     Returns ``(C_exact, C_out, absum)``, float64 arrays of shape [L][rows][N]
     (batch dim dropped when the inputs had none): the unrounded value, the value
     rounded once to ``out_dtype``, and sum_k |a_hat b_hat| for the error bound.
@@ -158,6 +175,10 @@ def scaled_gemm(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.n
         A = A[None]
         B = B[None]
     assert A.dtype == np.uint8 and B.dtype == np.uint8
+    if (a_fmt == FMT_E2M1) != (b_fmt == FMT_E2M1):
+        raise ValueError("FP4 operands go in pairs (A and B of the same dtype)")
+    if a_fmt == FMT_E2M1:
+        A, B = unpack_fp4(A), unpack_fp4(B)
     L, M, K = A.shape
     Lb, N, Kb = B.shape
     if Lb != L or Kb != K:
@@ -165,7 +186,7 @@ def scaled_gemm(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.n
     m0, m1 = rows if rows is not None else (0, M)
     sa = np.ascontiguousarray(scale_a)
     sb = np.ascontiguousarray(scale_b)
-    if scale_mode == SCALE_MX32_UE8M0:
+    if scale_mode in (SCALE_MX32_UE8M0, SCALE_NV16_E4M3):
         assert sa.dtype == np.uint8 and sb.dtype == np.uint8
     else:
         assert sa.dtype == np.float32 and sb.dtype == np.float32

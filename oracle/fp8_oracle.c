@@ -48,6 +48,7 @@
 
 #define OR_FMT_E4M3 0
 #define OR_FMT_E5M2 1
+#define OR_FMT_E2M1 2
 
 #define OR_OUT_F32 0
 #define OR_OUT_BF16 1
@@ -59,6 +60,7 @@
 #define OR_SCALE_A1x128_B1x128 1
 #define OR_SCALE_A1x128_B128x128 2
 #define OR_SCALE_MX32_UE8M0 3
+#define OR_SCALE_NV16_E4M3 4
 
 /* ------------------------------------------------------------------------ */
 /* FP8 decode, bit by bit.                                                   */
@@ -101,7 +103,22 @@ double oracle_decode_e5m2(uint8_t code) {
   return sign ? -mag : mag;
 }
 
+/* float4_e2m1 (cuDNN "GEMM + Amax (SM100)", Dtypes: float4_e2m1fn_x2, two
+ * values per byte): 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit, in
+ * the low four bits of `code`.
+ * Normal:    (1 + m/2) * 2^(e-1)  =  (2 + m) * 2^(e-2)
+ * Subnormal: (m/2)                =  m * 2^-1
+ * No infinity and no NaN; largest finite 6. */
+double oracle_decode_e2m1(uint8_t code) {
+  int sign = (code >> 3) & 1;
+  int e = (code >> 1) & 0x3;
+  int m = code & 0x1;
+  double mag = (e == 0) ? ldexp((double)m, -1) : ldexp((double)(2 + m), e - 2);
+  return sign ? -mag : mag;
+}
+
 double oracle_decode(int fmt, uint8_t code) {
+  if (fmt == OR_FMT_E2M1) return oracle_decode_e2m1(code);
   return fmt == OR_FMT_E5M2 ? oracle_decode_e5m2(code) : oracle_decode_e4m3(code);
 }
 
@@ -215,20 +232,24 @@ static double scale_128x128(const float *s, int64_t l, int64_t N, int64_t n, int
   return (double)s[(l * NB + n / 128) * KB + c];
 }
 
-/* MX scale factors in the physical atom layout of "GEMM + Amax (SM100)":
- * the logical tensor has shape (32, 4, ceil(MN/128), 4, ceil(K/128), L) and is
- * the physical C-contiguous (L, ceil(MN/128), ceil(K/128), 32, 4, 4) allocation
- * permuted by (3, 4, 1, 5, 2, 0).  Reading the logical modes with the first
- * index fastest, row r = i32 + 32*i4 + 128*mb and factor index f = j4 + 4*kb,
- * where factor f covers k in [32f, 32f + 32).  So the byte offset is
- * ((l*MB + mb)*KB + kb)*512 + i32*16 + i4*4 + j4. */
-static double scale_mx(const uint8_t *sf, int64_t l, int64_t rows, int64_t r, int64_t k, int64_t K) {
+/* Block scale factors in the physical atom layout of "GEMM + Amax (SM100)":
+ * with sf_vec_size v the logical tensor has shape
+ * (32, 4, ceil(MN/128), 4, ceil(K/(4v)), L) and is the physical C-contiguous
+ * (L, ceil(MN/128), ceil(K/(4v)), 32, 4, 4) allocation permuted by
+ * (3, 4, 1, 5, 2, 0).  Reading the logical modes with the first index
+ * fastest, row r = i32 + 32*i4 + 128*mb and factor index f = j4 + 4*kb, where
+ * factor f covers k in [v*f, v*f + v).  So the byte offset is
+ * ((l*MB + mb)*KB + kb)*512 + i32*16 + i4*4 + j4.  The factors are UE8M0
+ * for v = 32 and float8_e4m3fn for v = 16 (Dtypes: an E4M3 factor only with
+ * sf_vec_size 16). */
+static double scale_blocked(const uint8_t *sf, int64_t l, int64_t rows, int64_t r, int64_t k, int64_t K,
+                            int vec) {
   int64_t MB = (rows + 127) / 128;
-  int64_t KB = (K + 127) / 128;
+  int64_t KB = (K + 4 * vec - 1) / (4 * vec);
   int64_t mb = r / 128, rin = r % 128, i4 = rin / 32, i32 = rin % 32;
-  int64_t f = k / 32, kb = f / 4, j4 = f % 4;
+  int64_t f = k / vec, kb = f / 4, j4 = f % 4;
   int64_t off = ((l * MB + mb) * KB + kb) * 512 + i32 * 16 + i4 * 4 + j4;
-  return oracle_decode_ue8m0(sf[off]);
+  return vec == 16 ? oracle_decode_e4m3(sf[off]) : oracle_decode_ue8m0(sf[off]);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -254,11 +275,12 @@ static void one_element(const job_t *j, int64_t l, int64_t m, int64_t n, double 
     }
     c = (sa * sb) * acc;
     s = fabs(sa * sb) * aacc;
-  } else if (j->scale_mode == OR_SCALE_MX32_UE8M0) {
+  } else if (j->scale_mode == OR_SCALE_MX32_UE8M0 || j->scale_mode == OR_SCALE_NV16_E4M3) {
     /* A_hat = dequantize(A, SFA), B_hat likewise, C = sum_k A_hat * B_hat. */
+    const int vec = j->scale_mode == OR_SCALE_NV16_E4M3 ? 16 : 32;
     for (int64_t k = 0; k < K; ++k) {
-      double ah = j->dec_a[a[k * j->sAk]] * scale_mx((const uint8_t *)j->scale_a, l, j->M, m, k, K);
-      double bh = j->dec_b[b[k * j->sBk]] * scale_mx((const uint8_t *)j->scale_b, l, j->N, n, k, K);
+      double ah = j->dec_a[a[k * j->sAk]] * scale_blocked((const uint8_t *)j->scale_a, l, j->M, m, k, K, vec);
+      double bh = j->dec_b[b[k * j->sBk]] * scale_blocked((const uint8_t *)j->scale_b, l, j->N, n, k, K, vec);
       c += ah * bh;
       s += fabs(ah * bh);
     }
@@ -327,7 +349,8 @@ int oracle_scaled_gemm(int64_t L, int64_t M, int64_t N, int64_t K,
                        double *C_exact, double *C_out, double *absum,
                        int64_t m0, int64_t m1, int nthreads) {
   if (L < 0 || M < 0 || N < 0 || K < 0 || m0 < 0 || m1 > M || m0 > m1) return -1;
-  if (scale_mode < 0 || scale_mode > 3) return -1;
+  if (scale_mode < 0 || scale_mode > 4) return -1;
+  if (a_fmt < 0 || a_fmt > 2 || b_fmt < 0 || b_fmt > 2) return -1;
   if (out_dtype < 0 || out_dtype > 4) return -1;
   if (bias && (out_dtype == OR_OUT_E4M3 || out_dtype == OR_OUT_E5M2)) return -1; /* not defined by the pages */
   job_t *j = (job_t *)calloc(1, sizeof(job_t));

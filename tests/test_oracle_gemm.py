@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import library_refs
 import oracle
 from precision_matmul_gb300 import synth
 
@@ -276,32 +277,12 @@ def test_mx_factor_layout_through_page_permutation(facts):
     assert np.allclose(ab, refab, rtol=1e-12, atol=0)
 
 
-def _library_blocked_layout():
-    """torch's own routine that lays out MX scale factors for its block-scaled
-    matmul (the cuBLAS "D block scaling factors layout": 128-row by 4-factor
-    atoms).  Its module imports test-only packages, so the two functions are
-    compiled from torch's installed source by themselves."""
-    import ast
-    import importlib.util
-    spec = importlib.util.find_spec("torch.testing._internal.common_quantized")
-    if spec is None or spec.origin is None:
-        pytest.skip("torch ships no blocked-layout helper")
-    with open(spec.origin) as f:
-        tree = ast.parse(f.read())
-    fns = [n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name in ("ceil_div", "to_blocked")]
-    if len(fns) != 2:
-        pytest.skip("torch's blocked-layout helper not found")
-    ns = {"torch": torch}
-    exec(compile(ast.Module(body=fns, type_ignores=[]), spec.origin, "exec"), ns)
-    return ns["to_blocked"]
-
-
 def test_mx_factor_layout_matches_the_library_blocked_layout():
     # The row order inside one 128-row atom (row = i32 + 32*i4) is a reading of
     # the page's logical modes.  torch lays out the same hardware factors with
     # an implementation of its own; factors placed by it must give the oracle
     # the per-element dequantize-then-matmul result.
-    to_blocked = _library_blocked_layout()
+    to_blocked = library_refs.get("to_blocked")
     L, M, N, K = 2, 200, 136, 416  # ragged rows, factor columns padded to a multiple of 4
     p = synth.mx_batched(L=L, M=M, N=N, K=K, seed=62)
     a, b = p.a.numpy(), p.b.numpy()
