@@ -13,9 +13,10 @@ Definition evaluated (see the C file for the per-step citations)::
     C[l,m,n] = round_out( sum_c S_A(l,m,c) S_B(l,n,c) sum_{k in c} dec(A[l,m,k]) dec(B[l,n,k]) )
     Amax     = max |C|
 
-Sources: mmaemu "API reference (v0.1)" (mmaemu.scaled_mm); TileOPs "Linear
-Algebra Operators" (GemmFP8FwdOp scale forms); cuDNN "GEMM + Amax (SM100)"
-(Shapes, Equations, the physical scale-factor atom layout).
+Sources: mmaemu "API reference (v0.1)" (mmaemu.scaled_mm, including FP8
+outputs and scale_result); TileOPs "Linear Algebra Operators" (GemmFP8FwdOp
+scale forms and bias); cuDNN "GEMM + Amax (SM100)" (Shapes, Equations, Dtypes,
+the physical scale-factor atom layout, FP4 operands).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_*.py``.  The reading of the MX scale-factor row order inside

@@ -20,6 +20,10 @@
  *     sf_vec_size = 32 elements along K, then a plain sum over K, then
  *     Amax = max over m, n, l of |C|  (cuDNN "GEMM + Amax (SM100)", Shapes,
  *     Equations and the "Using JAX arrays" note on the physical atom layout).
+ *     The same page's FP4 operands (E2M1) with factors per 32 (UE8M0) or per
+ *     16 (float8_e4m3fn) elements follow the same steps.
+ *   - Optional bias [N] added before the rounding (TileOPs GemmFP8FwdOp), and
+ *     FP8 outputs scaled by scale_result (mmaemu.scaled_mm).
  *
  * Everything is evaluated in float64 with one final rounding to the output
  * format (round to nearest, ties to even).  For E4M3 operands every product is
@@ -38,7 +42,9 @@
  * casts; brute-force exact rationals on tiny K; power-of-two scale linearity;
  * NT/NN/TN/TT stride equivalence; constant block scales equal per-tensor; MX
  * factors read back through the page's logical-to-physical permutation;
- * output rounding against C's and numpy's conversions.
+ * output rounding against C's and numpy's conversions; FP8 outputs against
+ * torch's float8 casts; bias against exact rationals; FP4 against torch's
+ * own FP4 packing and blocked-layout routines.
  */
 #include <math.h>
 #include <pthread.h>
