@@ -25,7 +25,7 @@ from ._binding import (FP8MM_E4M3, FP8MM_E5M2, FP8MM_OUT_BF16, FP8MM_OUT_F16, FP
                        FP8MM_SCALE_TENSOR, FP8MMError, Plan, fp8mm_device_error, fp8mm_gemm, fp8mm_plan,
                        fp8mm_run, fp8mm_status_string, make_desc)
 
-__all__ = ["scaled_mm", "torch_scaled_mm", "describe", "plan_for", "Plan", "FP8MMError", "fp8mm_plan", "fp8mm_run", "fp8mm_gemm",
+__all__ = ["scaled_mm", "torch_scaled_mm", "bmm_fp8", "describe", "plan_for", "Plan", "FP8MMError", "fp8mm_plan", "fp8mm_run", "fp8mm_gemm",
            "fp8mm_device_error", "fp8mm_status_string", "make_desc", "FP8MM_E4M3", "FP8MM_E5M2",
            "FP8MM_OUT_F32", "FP8MM_OUT_BF16", "FP8MM_OUT_F16", "FP8MM_SCALE_TENSOR",
            "FP8MM_SCALE_A1x128_B1x128", "FP8MM_SCALE_A1x128_B128x128", "FP8MM_SCALE_MX32_UE8M0"]
@@ -260,3 +260,31 @@ def torch_scaled_mm(input, mat2, scale_a, scale_b, bias=None, scale_result=None,
     c, _ = scaled_mm(input, b, scale_a, scale_b, out_dtype=out_dtype, use_fast_accum=use_fast_accum,
                      scale_mode=FP8MM_SCALE_TENSOR, out=out, strict_torch=True)
     return c
+
+
+def bmm_fp8(a, b, scale_a, scale_b, *, trans_b=False, out_dtype=None, use_fast_accum=False, out=None):
+    """Batched FP8 GEMM d[i] = (a[i] @ b[i]) * scale_a * scale_b (TileOPs
+    "Linear Algebra Operators", BmmFP8FwdOp).
+
+    a is [B, M, K]; b is [B, K, N] (trans_b False, torch.bmm's order) or
+    [B, N, K] (trans_b True); scale_a and scale_b are per-tensor fp32 (0-dim or
+    one element); out_dtype defaults to bfloat16.  Whether b can be read in
+    place is decided by its strides, not by trans_b: the kernels read b with K
+    innermost, so a b whose [B, N, K] view is contiguous (a [B, N, K] tensor,
+    or the transpose of one given as [B, K, N]) is passed on without a copy.
+    Any other b raises ValueError (a transposing copy is not provided).
+    Returns d, [B, M, N] (use ``scaled_mm`` for the fused amax as well).
+    """
+    torch = _torch()
+    if out_dtype is None:
+        out_dtype = torch.bfloat16
+    if a.dim() != 3 or b.dim() != 3:
+        raise ValueError("a must be [B, M, K] and b [B, K, N] (or [B, N, K] with trans_b)")
+    bnk = b if trans_b else b.transpose(1, 2)
+    if bnk.shape[0] != a.shape[0] or bnk.shape[2] != a.shape[2]:
+        raise ValueError("a and b disagree on the batch or on K")
+    if not bnk.is_contiguous():
+        raise ValueError("b is not K-innermost; a transposing copy is not provided")
+    d, _ = scaled_mm(a, bnk, scale_a.reshape(1), scale_b.reshape(1), out_dtype=out_dtype,
+                     use_fast_accum=use_fast_accum, scale_mode=FP8MM_SCALE_TENSOR, out=out)
+    return d

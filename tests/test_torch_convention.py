@@ -1,4 +1,4 @@
-"""The torch._scaled_mm calling convention on the host (CPU only).
+"""The torch._scaled_mm and batched (BmmFP8FwdOp) calling conventions on the host (CPU only).
 
 ``torch_scaled_mm`` only rearranges arguments for ``scaled_mm``: mat2 [K, N]
 column-major becomes the [N, K] K-contiguous operand (same storage), the
@@ -72,3 +72,33 @@ def test_e5m2_pair_is_sent_with_torchs_refusal(calls):
     a, w, sa, sb = _operands(fa=torch.float8_e5m2, fb=torch.float8_e5m2)
     pm.torch_scaled_mm(a, w.t(), sa, sb, out_dtype=torch.bfloat16)
     assert calls[-1][4]["strict_torch"] is True
+
+
+def test_bmm_b_in_either_axis_order_is_read_in_place(calls):
+    g = torch.Generator().manual_seed(8)
+    a = torch.randn(3, 16, 64, generator=g).to(torch.float8_e4m3fn)
+    w = torch.randn(3, 24, 64, generator=g).to(torch.float8_e4m3fn)     # [B, N, K]
+    sa, sb = torch.tensor(0.5), torch.tensor(2.0)                        # 0-dim, as the page states
+    pm.bmm_fp8(a, w, sa, sb, trans_b=True)
+    pm.bmm_fp8(a, w.transpose(1, 2), sa, sb)                             # [B, K, N] view of the same storage
+    for a2, b2, sa2, sb2, kw in calls:
+        assert a2 is a and b2.shape == (3, 24, 64) and b2.is_contiguous() and b2.data_ptr() == w.data_ptr()
+        assert sa2.shape == (1,) and sb2.shape == (1,) and float(sa2) == 0.5 and float(sb2) == 2.0
+        assert kw["scale_mode"] == pm.FP8MM_SCALE_TENSOR and kw["out_dtype"] == torch.bfloat16
+        assert kw["use_fast_accum"] is False
+
+
+def test_bmm_refuses_k_outermost_b_and_bad_shapes(calls):
+    g = torch.Generator().manual_seed(9)
+    a = torch.randn(3, 16, 64, generator=g).to(torch.float8_e4m3fn)
+    bkn = torch.randn(3, 64, 24, generator=g).to(torch.float8_e4m3fn)   # [B, K, N] with N innermost
+    s = torch.tensor(1.0)
+    with pytest.raises(ValueError):
+        pm.bmm_fp8(a, bkn, s, s)
+    with pytest.raises(ValueError):
+        pm.bmm_fp8(a, bkn.transpose(1, 2).contiguous(), s, s)           # [B, N, K] without trans_b
+    with pytest.raises(ValueError):
+        pm.bmm_fp8(a[:2], bkn.transpose(1, 2).contiguous(), s, s, trans_b=True)
+    with pytest.raises(ValueError):
+        pm.bmm_fp8(a[0], bkn[0], s, s)
+    assert not calls

@@ -34,3 +34,15 @@ def test_e5m2_pair_is_refused_like_torch():
     c, _ = pm.scaled_mm(a, w, sa, sb, out_dtype=torch.bfloat16)  # the library's own call computes it
     torch.cuda.synchronize()
     assert c.shape == (200, 264)
+
+
+def test_bmm_same_bits_as_scaled_mm():
+    g = torch.Generator().manual_seed(32)
+    a = (torch.randn(2, 136, 256, generator=g) * 20).clamp(-448, 448).to(torch.float8_e4m3fn).cuda()
+    w = (torch.randn(2, 200, 256, generator=g) * 20).clamp(-448, 448).to(torch.float8_e4m3fn).cuda()
+    sa, sb = torch.tensor(0.5, device="cuda"), torch.tensor(0.125, device="cuda")
+    d = pm.bmm_fp8(a, w.transpose(1, 2), sa, sb)                 # b as torch.bmm's [B, K, N] view
+    ref, _ = pm.scaled_mm(a, w, sa.reshape(1), sb.reshape(1), out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert d.shape == (2, 136, 200)
+    assert torch.equal(d.view(torch.int16), ref.view(torch.int16))
