@@ -159,3 +159,21 @@ def test_plan_for_builds_one_descriptor_per_key(monkeypatch):
     assert (d.splitk, d.swap_ab, d.block_n, d.device, d.cta_pair, d.epi_warps, d.stages, d.strict_torch) == \
         (3, 2, 64, 0, 2, 0, 0, 0)
     assert (e.epi_warps, e.strict_torch) == (16, 1)
+
+
+def test_a_failed_plan_raises_and_is_not_cached(monkeypatch):
+    # Without a GPU the library's device query fails: fp8mm_plan returns
+    # FP8MM_ERR_CUDA, the binding raises, and nothing is cached for the key,
+    # so a later call plans afresh instead of reusing a broken plan.
+    from precision_matmul_gb300 import _binding as B
+    from precision_matmul_gb300 import build as cuda_build
+    if torch.cuda.is_available():
+        pytest.skip("needs a host without a GPU")
+    cuda_build.build()
+    monkeypatch.setattr(pm, "_plans", {})
+    key = (64, 64, 128, 1, 0, 0, 0, 1, 1, 0, 0, 0, 0)
+    for _ in range(2):
+        with pytest.raises(pm.FP8MMError) as e:
+            pm.plan_for(key)
+        assert e.value.status == B.FP8MM_ERR_CUDA
+        assert pm._plans == {}
