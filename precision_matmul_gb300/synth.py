@@ -23,13 +23,14 @@ import dataclasses
 import torch
 
 E4M3, E5M2 = 0, 1
-OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
+OUT_F32, OUT_BF16, OUT_F16, OUT_E4M3, OUT_E5M2 = 0, 1, 2, 3, 4
 SCALE_TENSOR, SCALE_A1x128_B1x128, SCALE_A1x128_B128x128, SCALE_MX32_UE8M0 = 0, 1, 2, 3
 
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 TORCH_FP8 = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
-OUT_TORCH = {OUT_F32: torch.float32, OUT_BF16: torch.bfloat16, OUT_F16: torch.float16}
-OUT_NAME = {OUT_F32: "f32", OUT_BF16: "bf16", OUT_F16: "f16"}
+OUT_TORCH = {OUT_F32: torch.float32, OUT_BF16: torch.bfloat16, OUT_F16: torch.float16,
+             OUT_E4M3: torch.float8_e4m3fn, OUT_E5M2: torch.float8_e5m2}
+OUT_NAME = {OUT_F32: "f32", OUT_BF16: "bf16", OUT_F16: "f16", OUT_E4M3: "e4m3", OUT_E5M2: "e5m2"}
 
 
 @dataclasses.dataclass
@@ -94,30 +95,33 @@ def tiny_per_tensor(M=256, N=256, K=256, seed=0) -> Problem:
                    E4M3, E4M3, SCALE_TENSOR, OUT_F32, True)
 
 
-def llm_per_tensor(M=4096, N=4096, K=4096, seed=1, fast_accum=True, out_dtype=OUT_BF16) -> Problem:
-    """N(0,1)*112 codes, E4M3, scales 2^U(-4,4), bf16 out; fast or slow accumulation."""
+def llm_per_tensor(M=4096, N=4096, K=4096, seed=1, fast_accum=True, out_dtype=OUT_BF16, L=1) -> Problem:
+    """N(0,1)*112 codes, E4M3, scales 2^U(-4,4), bf16 out; fast or slow accumulation.
+    L > 1 draws a batch of L problems sharing the two per-tensor scales (the
+    L = 1 draw is the first slice of the same stream)."""
     g = _gen(seed)
-    a = cast_fp8(torch.randn(M, K, generator=g) * (448.0 / 4), E4M3)
-    b = cast_fp8(torch.randn(N, K, generator=g) * (448.0 / 4), E4M3)
+    a = cast_fp8(torch.randn(L, M, K, generator=g) * (448.0 / 4), E4M3)
+    b = cast_fp8(torch.randn(L, N, K, generator=g) * (448.0 / 4), E4M3)
     sa = _log_uniform(g, (1,), -4, 4)
     sb = _log_uniform(g, (1,), -4, 4)
-    return Problem("llm_per_tensor", 1, M, N, K, a[None], b[None], sa, sb,
+    return Problem("llm_per_tensor", L, M, N, K, a, b, sa, sb,
                    E4M3, E4M3, SCALE_TENSOR, out_dtype, fast_accum)
 
 
-def blockwise(M=8192, N=7168, K=2048, seed=2, b_block=128, out_dtype=OUT_BF16) -> Problem:
-    """U(-448,448) codes; A scales per 1x128, B per 128x128 (or 1x128); 2^U(-8,8); slow."""
+def blockwise(M=8192, N=7168, K=2048, seed=2, b_block=128, out_dtype=OUT_BF16, L=1) -> Problem:
+    """U(-448,448) codes; A scales per 1x128, B per 128x128 (or 1x128); 2^U(-8,8); slow.
+    L > 1 draws a batch with scales per batch ([L][..][..])."""
     g = _gen(seed)
-    a = cast_fp8((torch.rand(M, K, generator=g) * 2 - 1) * 448.0, E4M3)
-    b = cast_fp8((torch.rand(N, K, generator=g) * 2 - 1) * 448.0, E4M3)
-    sa = _log_uniform(g, (1, M, _kb(K)), -8, 8)
+    a = cast_fp8((torch.rand(L, M, K, generator=g) * 2 - 1) * 448.0, E4M3)
+    b = cast_fp8((torch.rand(L, N, K, generator=g) * 2 - 1) * 448.0, E4M3)
+    sa = _log_uniform(g, (L, M, _kb(K)), -8, 8)
     if b_block == 128:
-        sb = _log_uniform(g, (1, (N + 127) // 128, _kb(K)), -8, 8)
+        sb = _log_uniform(g, (L, (N + 127) // 128, _kb(K)), -8, 8)
         mode = SCALE_A1x128_B128x128
     else:
-        sb = _log_uniform(g, (1, N, _kb(K)), -8, 8)
+        sb = _log_uniform(g, (L, N, _kb(K)), -8, 8)
         mode = SCALE_A1x128_B1x128
-    return Problem("blockwise", 1, M, N, K, a[None], b[None], sa, sb,
+    return Problem("blockwise", L, M, N, K, a, b, sa, sb,
                    E4M3, E4M3, mode, out_dtype, False)
 
 

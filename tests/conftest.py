@@ -28,3 +28,21 @@ def page_facts():
 @pytest.fixture(scope="session")
 def facts():
     return page_facts()
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print how close each parity case came to its bound (worst error / bound)."""
+    mod = sys.modules.get("parity")
+    report = getattr(mod, "REPORT", None) if mod else None
+    if not report:
+        return
+    tr = terminalreporter
+    tr.section("parity: worst |C_gpu - C_exact| / bound per case")
+    for name, worst, count in sorted(report, key=lambda x: -x[1]):
+        tr.write_line(f"{worst:10.3e}  {count:>12d} elements  {name}")
+    path = os.environ.get("PARITY_REPORT")
+    if path:
+        import json
+        with open(path, "w") as f:
+            for name, worst, count in report:
+                f.write(json.dumps({"test": name, "worst_ratio": worst, "elements": count}) + "\n")

@@ -250,3 +250,52 @@ def test_plan_preview_matches_device_plan(shape):
     keys = ("swap_ab", "block_n", "splitk", "stages", "units", "slow", "smem_bytes", "cta_pair", "epi_warps")
     assert {k: pre[k] for k in keys} == {k: got[k] for k in keys}
 
+
+
+@pytest.mark.parametrize("fast", [True, False])
+@pytest.mark.parametrize("L,M,N,K", [(2, 256, 384, 512), (3, 200, 264, 400)])
+def test_per_tensor_batched(L, M, N, K, fast):
+    # a batch of per-tensor GEMMs: the batch stride of the tensor maps and of the scheduler's units
+    p = synth.llm_per_tensor(L=L, M=M, N=N, K=K, seed=40 + L, fast_accum=fast)
+    _run_check(p)
+
+
+@pytest.mark.parametrize("mode", [synth.SCALE_A1x128_B128x128, synth.SCALE_A1x128_B1x128])
+@pytest.mark.parametrize("L,M,N,K", [(2, 272, 392, 640), (3, 136, 520, 384)])
+def test_blockwise_batched(L, M, N, K, mode):
+    # per-batch block scales ([L][..][..]) on ragged shapes
+    p = synth.blockwise(L=L, M=M, N=N, K=K, seed=42 + L, b_block=128 if mode == synth.SCALE_A1x128_B128x128 else 1)
+    _run_check(p)
+
+
+@pytest.mark.parametrize("knobs", [dict(swap_ab=1, splitk=2), dict(block_n=256, swap_ab=2),
+                                   dict(cta_pair=1, swap_ab=2, block_n=128)])
+def test_batched_plan_forms(knobs):
+    # swapped, 256-column held and CTA-pair tiles over a batch
+    p = synth.llm_per_tensor(L=2, M=72 if knobs.get("swap_ab") == 1 else 264, N=392, K=768, seed=44,
+                             fast_accum=knobs.get("block_n") != 256)
+    _run_check(p, **knobs)
+
+
+def test_bmm_fp8_against_oracle():
+    # TileOPs BmmFP8FwdOp's convention, d[i] = (a[i] @ b[i]) * s_a * s_b, compared with the oracle
+    p = synth.llm_per_tensor(L=3, M=136, N=200, K=256, seed=45, fast_accum=False)
+    dev = torch.device("cuda:0")
+    a = p.a.to(dev).view(torch.float8_e4m3fn)
+    w = p.b.to(dev).view(torch.float8_e4m3fn)                    # [B, N, K]
+    sa, sb = p.scale_a.to(dev).reshape(()), p.scale_b.to(dev).reshape(())
+    d = pm.bmm_fp8(a, w.transpose(1, 2), sa, sb, use_fast_accum=False)   # b given as [B, K, N]
+    torch.cuda.synchronize()
+    assert d.shape == (3, 136, 200)
+    check(p, d, torch.tensor([0.0]), full_amax=False)
+
+
+def test_torch_scaled_mm_against_oracle():
+    p = synth.llm_per_tensor(M=200, N=264, K=384, seed=46, fast_accum=True, out_dtype=synth.OUT_F32)
+    dev = torch.device("cuda:0")
+    a = p.a[0].to(dev).view(torch.float8_e4m3fn)
+    w = p.b[0].to(dev).view(torch.float8_e4m3fn)
+    c = pm.torch_scaled_mm(a, w.t(), p.scale_a.to(dev), p.scale_b.to(dev), out_dtype=torch.float32,
+                           use_fast_accum=True)
+    torch.cuda.synchronize()
+    check(p, c, torch.tensor([0.0]), full_amax=False)

@@ -121,3 +121,22 @@ def test_strict_torch_refuses_what_torch_refuses(lib, fa, fb, mode, st):
 def test_strict_torch_flag_values(lib):
     assert status(512, 1024, 1024, out_dtype=0, strict_torch=2) == B.FP8MM_ERR_INVALID
     assert status(512, 1024, 1024, out_dtype=0, strict_torch=-1) == B.FP8MM_ERR_INVALID
+
+
+def test_every_fuzz_case_finds_an_accepted_plan(lib):
+    # the GPU fuzz redraws plan overrides until the library accepts them; on the host
+    # planner (152 SMs, 227 KiB of shared memory) each case must get there quickly
+    import test_gpu_fuzz as fz
+    for i in range(96):
+        p, knobs, r = fz._case(i)
+        for tries in range(200):
+            d = B.make_desc(p.M, p.N, p.K, p.L, a_fmt=p.a_fmt, b_fmt=p.b_fmt, scale_mode=p.scale_mode,
+                            out_dtype=p.out_dtype, fast_accum=1 if p.fast_accum else 0, **knobs)
+            try:
+                B.fp8mm_plan_preview(d, 152, 232448)
+                break
+            except B.FP8MMError as e:
+                assert e.status == B.FP8MM_ERR_UNSUPPORTED
+                knobs = fz._draw_knobs(r)
+        else:
+            raise AssertionError(f"case {i}: no accepted override set")
