@@ -24,7 +24,7 @@ def _describe(p, **kw):
 
 @pytest.mark.parametrize("i", range(96))
 def test_every_fuzz_case_is_accepted(i):
-    p, _ = _case(i)
+    p, _, _ = _case(i)
     L, M, N, K, fa, fb, mode, oc, shape = _describe(p)
     assert (L, M, N, K, fa, fb, mode) == (p.L, p.M, p.N, p.K, p.a_fmt, p.b_fmt, p.scale_mode)
     assert shape == (p.L, p.M, p.N)
