@@ -1,19 +1,31 @@
 """Benchmark of the FP8 scaled GEMM + amax hot path on GB300.
 
-Default workload (one "step"): the per-tensor E4M3 GEMM at LLM linear-layer
-size, M = N = K = 4096, NT, bf16 out + amax, run once with fast accumulation
-and once with slow accumulation (128-K chunks).  Other workloads with
---workload (tiny, blockwise, mx_e4m3, mx_e5m2, skinny_<M>[_adv]).
+One "step" (the default workload, ``all``) is one call of every workload the
+metric is quoted on, each with its own synthetic inputs resident in HBM:
 
-Prints ONE JSON line (rank 0).  `value` is whole-job TFLOP/s with inputs
-resident in HBM; `e2e` is the same metric through the public API with the
-operands copied from pinned host memory and C read back every step.
-`--impl reference` times the CPU oracle instead (a bounded sample of the
-workload on the host cores).
+  c1    per-tensor E4M3 256^3, fp32 out, fast accumulation
+  c2    per-tensor E4M3 4096^3 NT, bf16 out, fast and slow accumulation
+  c3    E4M3 8192 x 7168 x 2048, A 1x128 / B 128x128 fp32 scales, slow, bf16 out
+  c4    MX batch 4 x 4096^3 (UE8M0 per 32 along K), fp32 out, E4M3 and E5M2
+  c5    skinny N = 28672, K = 8192, M in {16, 64, 256, 1024, 2048, 8192},
+        per-tensor E4M3 gauss40, bf16 out, fast and slow accumulation
+
+every call with the fused amax.  ``value`` is the whole step's TFLOP/s (all
+calls' flops over the sum of their device times); ``per_config`` reports every
+call against its own roofline (tensor-bound: of the FP8 peak; HBM-bound: of
+the copy bandwidth); ``roofline`` is the dominant call of the step.  ``e2e``
+is the same metric through the public API with each call's operands copied
+from pinned host memory and C and amax read back, inside the timed region.
+``--impl reference`` times the CPU oracle instead (a bounded sample of every
+call on the host cores).  Subsets with ``--workload`` (comma-separated names
+or groups: c1 .. c5, mx, skinny, or a single call name).
+
+Prints ONE JSON line (rank 0).
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -28,7 +40,9 @@ if ROOT not in sys.path:
 METRIC = "FP8 scaled-GEMM TFLOP/s (+GB/s) at 1 GB300 and % of FP8/HBM roofline"
 KERNEL_SOURCES = ["precision_matmul_gb300/csrc/fp8mm_kernel.cuh", "precision_matmul_gb300/csrc/ptx.cuh"]
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
+FP8_NOMINAL_TFLOPS = 4500.0
 L2_BYTES = 129 * 10 ** 6
+SKINNY_M = (16, 64, 256, 1024, 2048, 8192)
 
 
 def kernel_hash() -> str:
@@ -39,37 +53,85 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def problems(name: str):
+# name -> (description, factory); factories sharing a key in `_SHARED` reuse one input draw
+def _catalogue():
     from precision_matmul_gb300 import synth
-    if name == "llm_4096":
-        return [synth.llm_per_tensor(fast_accum=True), synth.llm_per_tensor(fast_accum=False)]
-    if name == "llm_4096_fast":
-        return [synth.llm_per_tensor(fast_accum=True)]
-    if name == "llm_4096_slow":
-        return [synth.llm_per_tensor(fast_accum=False)]
-    if name == "tiny":
-        return [synth.tiny_per_tensor()]
-    if name == "blockwise":
-        return [synth.blockwise()]
-    if name == "mx_e4m3":
-        return [synth.mx_batched(fmt=synth.E4M3)]
-    if name == "mx_e5m2":
-        return [synth.mx_batched(fmt=synth.E5M2)]
-    if name.startswith("skinny_"):
-        parts = name.split("_")
-        M = int(parts[1])
-        data = "adversarial" if len(parts) > 2 and parts[2] == "adv" else "gauss40"
-        return [synth.skinny(M=M, data=data, fast_accum=True), synth.skinny(M=M, data=data, fast_accum=False)]
-    raise SystemExit(f"unknown workload {name}")
+    cat = {
+        "c1_tiny_256": ("per-tensor E4M3 256^3, fp32 out, fast", lambda: synth.tiny_per_tensor()),
+        "c2_llm4096_fast": ("per-tensor E4M3 4096^3 NT, bf16 out, fast",
+                            lambda: synth.llm_per_tensor(fast_accum=True)),
+        "c2_llm4096_slow": ("per-tensor E4M3 4096^3 NT, bf16 out, slow (128-K chunks)",
+                            lambda: synth.llm_per_tensor(fast_accum=False)),
+        "c3_blockwise": ("E4M3 8192x7168x2048, A 1x128 / B 128x128 fp32 scales, slow, bf16 out",
+                         lambda: synth.blockwise()),
+        "c4_mx_e4m3": ("MX 4 x 4096^3 E4M3, UE8M0 per 32 along K, fp32 out",
+                       lambda: synth.mx_batched(fmt=synth.E4M3)),
+        "c4_mx_e5m2": ("MX 4 x 4096^3 E5M2, UE8M0 per 32 along K, fp32 out",
+                       lambda: synth.mx_batched(fmt=synth.E5M2)),
+    }
+    for M in SKINNY_M:
+        for fast in (True, False):
+            mode = "fast" if fast else "slow"
+            cat[f"c5_skinny_M{M}_{mode}"] = (f"per-tensor E4M3 M={M} N=28672 K=8192 gauss40, bf16 out, {mode}",
+                                             (M, "gauss40", fast))
+            cat[f"c5_skinny_M{M}_adv_{mode}"] = (
+                f"per-tensor E4M3 M={M} N=28672 K=8192 adversarial, bf16 out, {mode}", (M, "adversarial", fast))
+    return cat
 
 
-WORKLOAD_DESC = {
-    "llm_4096": "per-tensor E4M3 GEMM M=N=K=4096 NT, bf16 out + amax, fast then slow accumulation",
-    "tiny": "per-tensor E4M3 GEMM M=N=K=256, fp32 out + amax, fast accumulation",
-    "blockwise": "E4M3 GEMM M=8192 N=7168 K=2048, A 1x128 / B 128x128 fp32 scales, slow, bf16 out + amax",
-    "mx_e4m3": "MX block-scaled batched GEMM L=4 x 4096^3 E4M3, UE8M0 per 32 along K, fp32 out + amax",
-    "mx_e5m2": "MX block-scaled batched GEMM L=4 x 4096^3 E5M2, UE8M0 per 32 along K, fp32 out + amax",
+DEFAULT = (["c1_tiny_256", "c2_llm4096_fast", "c2_llm4096_slow", "c3_blockwise", "c4_mx_e4m3", "c4_mx_e5m2"] +
+           [f"c5_skinny_M{M}_{m}" for M in SKINNY_M for m in ("fast", "slow")])
+GROUPS = {
+    "all": DEFAULT,
+    "c1": ["c1_tiny_256"], "tiny": ["c1_tiny_256"],
+    "c2": ["c2_llm4096_fast", "c2_llm4096_slow"], "llm_4096": ["c2_llm4096_fast", "c2_llm4096_slow"],
+    "llm_4096_fast": ["c2_llm4096_fast"], "llm_4096_slow": ["c2_llm4096_slow"],
+    "c3": ["c3_blockwise"], "blockwise": ["c3_blockwise"],
+    "c4": ["c4_mx_e4m3", "c4_mx_e5m2"], "mx": ["c4_mx_e4m3", "c4_mx_e5m2"],
+    "mx_e4m3": ["c4_mx_e4m3"], "mx_e5m2": ["c4_mx_e5m2"],
+    "c5": [f"c5_skinny_M{M}_{m}" for M in SKINNY_M for m in ("fast", "slow")],
 }
+for _M in SKINNY_M:
+    GROUPS[f"skinny_{_M}"] = [f"c5_skinny_M{_M}_fast", f"c5_skinny_M{_M}_slow"]
+    GROUPS[f"skinny_{_M}_adv"] = [f"c5_skinny_M{_M}_adv_fast", f"c5_skinny_M{_M}_adv_slow"]
+
+
+def workload_names(spec: str) -> list:
+    names = []
+    cat = _catalogue()
+    for part in spec.split(","):
+        part = part.strip()
+        got = GROUPS.get(part, [part] if part in cat else None)
+        if got is None:
+            raise SystemExit(f"unknown workload {part}")
+        names += [n for n in got if n not in names]
+    return names
+
+
+def problems(spec: str):
+    """(name, description, Problem) per call; fast/slow pairs of one skinny draw share inputs."""
+    from precision_matmul_gb300 import synth
+    cat = _catalogue()
+    shared = {}
+    out = []
+    for name in workload_names(spec):
+        desc, f = cat[name]
+        if callable(f):
+            p = f()
+        else:
+            M, data, fast = f
+            if (M, data) not in shared:
+                shared[(M, data)] = synth.skinny(M=M, data=data)
+            p = dataclasses.replace(shared[(M, data)], fast_accum=fast)
+        out.append((name, desc, p))
+    return out
+
+
+def config_of(spec: str, probs) -> dict:
+    """The `config` object both arms print."""
+    return {"workload": spec if spec != "all" else "every metric configuration: " + ", ".join(n for n, _, _ in probs),
+            "calls_per_step": len(probs),
+            "calls": [{"name": n, "M": p.M, "N": p.N, "K": p.K, "L": p.L} for n, _, p in probs]}
 
 
 def read_peaks():
@@ -83,17 +145,17 @@ def read_peaks():
 
 
 def read_traffic():
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
-    only if it was captured on the current kernel sources and this workload."""
+    """DRAM bytes per launch from the committed ncu summary, keyed by call
+    name, only if it was captured on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "fp8mm_kernel_traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
         if t.get("kernel_sources_sha256_16") == kernel_hash():
-            return t
+            return t.get("traffic_bytes_per_launch", {})
     except Exception:
         pass
-    return None
+    return {}
 
 
 class ClockSampler:
@@ -181,19 +243,20 @@ class ClockSampler:
 
 
 def oracle_sample(probs, target_s=8.0, max_rows=None):
-    """Time the CPU oracle on a bounded row sample of each problem; TFLOP/s."""
+    """Time the CPU oracle on a bounded row sample of each problem (batch 0,
+    all N); returns (TFLOP/s, threads, description)."""
     import oracle
     threads = os.cpu_count() or 1
     total_flops, total_t, descr = 0.0, 0.0, []
-    for p in probs:
+    for name, _, p in probs:
         a, b, sa, sb = p.a.numpy(), p.b.numpy(), p.scale_a.numpy(), p.scale_b.numpy()
-        rows = 8
+        rows = 4
         while True:
             t0 = time.perf_counter()
             oracle.scaled_gemm(a[:1], b[:1], sa, sb, a_fmt=p.a_fmt, b_fmt=p.b_fmt,
                                scale_mode=p.scale_mode, out_dtype=p.out_dtype, rows=(0, rows), nthreads=threads)
             dt = time.perf_counter() - t0
-            if dt > 0.5 or rows >= p.M:
+            if dt > 0.2 or rows >= p.M:
                 break
             rows = min(p.M, rows * 4)
         per_row = dt / rows
@@ -206,8 +269,9 @@ def oracle_sample(probs, target_s=8.0, max_rows=None):
         dt = time.perf_counter() - t0
         total_t += dt
         total_flops += 2.0 * want * p.N * p.K
-        descr.append(f"{p.name}: rows 0..{want} of M={p.M} (all N={p.N}, K={p.K}, batch 0)")
-    return total_flops / total_t / 1e12, threads, "; ".join(descr)
+        descr.append(f"{name}: rows 0..{want} of M={p.M}")
+    return total_flops / total_t / 1e12, threads, ("oracle on the first rows of batch 0 of every call (all N, all K), "
+                                                   "rate extrapolated by flops: " + "; ".join(descr))
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -233,21 +297,48 @@ def run_reference(args, rank, world):
     probs = problems(args.workload)
     vals = []
     for _ in range(args.warmup):
-        oracle_sample(probs, target_s=2.0)
+        oracle_sample(probs, target_s=1.0)
     sample = ""
+    cores = os.cpu_count()
     for _ in range(args.steps):
         v, cores, sample = oracle_sample(probs, target_s=max(2.0, 60.0 / max(1, args.steps)))
         vals.append(v)
     value = statistics.median(vals)
-    flops = sum(p.flops for p in probs)
+    flops = sum(p.flops for _, _, p in probs)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": flops / (value * 1e12) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD_DESC.get(args.workload, args.workload)},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "data": "synthetic", "config": config_of(args.workload, probs),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def cublas_fp8_peak(dev):
+    """torch._scaled_mm (cuBLAS) on a per-tensor E4M3 8192^3 GEMM, bf16 out,
+    fast accumulation: best of 10 back-to-back calls (a reference point for
+    the FP8 tensor peak, not the roofline denominator)."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).clamp(-448, 448).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).clamp(-448, 448).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b.t(), one, one, out_dtype=torch.bfloat16, use_fast_accum=True)
+        best = 1e9
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b.t(), one, one, out_dtype=torch.bfloat16, use_fast_accum=True)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        del a, b
+        return 2.0 * n ** 3 / best / 1e12
+    except Exception as e:  # not fatal: it is context only
+        return f"unavailable: {type(e).__name__}: {e}"
 
 
 def run_ours(args, rank, world, local_rank):
@@ -259,9 +350,12 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     probs = problems(args.workload)
     ins = []
-    for p in probs:
-        a, b = p.a.to(dev), p.b.to(dev)
-        sa, sb = p.scale_a.to(dev), p.scale_b.to(dev)
+    dev_inputs = {}
+    for name, _, p in probs:
+        key = id(p.a)
+        if key not in dev_inputs:  # fast/slow calls of one draw share their device operands
+            dev_inputs[key] = (p.a.to(dev), p.b.to(dev), p.scale_a.to(dev), p.scale_b.to(dev))
+        a, b, sa, sb = dev_inputs[key]
         squeeze = p.L == 1
         if squeeze:
             a, b = a[0], b[0]
@@ -312,27 +406,44 @@ def run_ours(args, rank, world, local_rank):
     for i, e0, e1 in evs:
         per_call[i].append(e0.elapsed_time(e1) / 1e3)
     step_s = max_over_ranks(sum(sum(x) for x in per_call) / args.steps, world, dev)
-    flops = sum(p.flops for p in probs)
+    flops = sum(p.flops for _, _, p in probs)
     value = whole_job_tflops(flops, step_s, world)
     err = pm.fp8mm_device_error(local_rank)
     if err:
         raise SystemExit(f"device abort recorded: {err:#x}")
 
+    # ---- sustained: the dominant call back to back for >= sustain_s under the clock sampler
+    call_s = [sum(x) / len(x) for x in per_call]
+    dom = max(range(len(probs)), key=lambda i: call_s[i])
+    sus_idx = next((i for i, (n, _, _) in enumerate(probs) if n == "c2_llm4096_slow"), dom)
+    sustained = None
+    if args.sustain_s > 0:
+        n_calls = max(10, int(args.sustain_s / max(call_s[sus_idx], 1e-6)))
+        for _ in range(5):
+            call(ins[sus_idx])
+        torch.cuda.synchronize()
+        with ClockSampler(local_rank) as sclk:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n_calls):
+                call(ins[sus_idx])
+            e1.record(stream)
+            torch.cuda.synchronize()
+        s_s = e0.elapsed_time(e1) / 1e3
+        sustained = {"call": probs[sus_idx][0], "calls": n_calls, "seconds": s_s,
+                     "tflops": probs[sus_idx][2].flops * n_calls / s_s / 1e12, "clocks": sclk.summary(),
+                     "note": "back to back, no L2 flush (the operands stay in L2)"}
+
     # ---- e2e through the public API: pinned host operands in, C and amax out
     host = []
     for p, a, b, sa, sb, c, amax in ins:
-        ha = a.cpu().pin_memory()
-        hb = b.cpu().pin_memory()
-        hsa, hsb = sa.cpu().pin_memory(), sb.cpu().pin_memory()
-        hc = torch.empty(c.shape, dtype=c.dtype).pin_memory()
-        hm = torch.empty(1, dtype=torch.float32).pin_memory()
-        host.append((p, ha, hb, hsa, hsb, hc, hm))
-    h2d = sum(x[1].numel() * x[1].element_size() + x[2].numel() * x[2].element_size() +
-              x[3].numel() * 4 + x[4].numel() * 4 for x in host)
-    d2h = sum(x[5].numel() * x[5].element_size() + 4 for x in host)
+        host.append((a.cpu().pin_memory(), b.cpu().pin_memory(), sa.cpu().pin_memory(), sb.cpu().pin_memory(),
+                     torch.empty(c.shape, dtype=c.dtype).pin_memory(), torch.empty(1, dtype=torch.float32).pin_memory()))
+    h2d = sum(sum(t.numel() * t.element_size() for t in x[:4]) for x in host)
+    d2h = sum(x[4].numel() * x[4].element_size() + 4 for x in host)
 
     def e2e_step():
-        for (p, ha, hb, hsa, hsb, hc, hm), (_, a, b, sa, sb, c, amax) in zip(host, ins):
+        for (ha, hb, hsa, hsb, hc, hm), (p, a, b, sa, sb, c, amax) in zip(host, ins):
             a.copy_(ha, non_blocking=True)
             b.copy_(hb, non_blocking=True)
             sa.copy_(hsa, non_blocking=True)
@@ -341,7 +452,7 @@ def run_ours(args, rank, world, local_rank):
             hc.copy_(c, non_blocking=True)
             hm.copy_(amax, non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
+    for _ in range(max(1, min(args.warmup, 3))):
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -350,56 +461,62 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3 / args.steps
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world, dev)
     e2e_value = world * flops / e2e_s / 1e12
 
     if rank != 0:
         return
-    # ---- roofline of the dominant kernel: the call with the largest share of the step
+    # ---- per-call rooflines and the dominant call's
     hbm, bf16, bf16_sus, peak_src = read_peaks()
     fp8_peak = bf16 * FP8_PER_BF16
-    plans = [pm.plan_for((p.M, p.N, p.K, p.L, p.a_fmt, p.b_fmt, p.scale_mode, p.out_dtype,
-                          1 if p.fast_accum else 0, 0, 0, 0, local_rank, 0)) for p in probs]
-    launches = sum(pl.kernel_launches() for pl in plans)
-    call_s = [sum(x) / len(x) for x in per_call]
-    dom = max(range(len(probs)), key=lambda i: call_s[i])
-    algo_flops, algo_bytes = plans[dom].roofline()
-    dom_s = call_s[dom]
-    t_roof = max(algo_flops / (fp8_peak * 1e12), algo_bytes / (hbm * 1e9))
-    bound = "tensor" if algo_flops / (fp8_peak * 1e12) >= algo_bytes / (hbm * 1e9) else "hbm"
+    cublas = cublas_fp8_peak(dev) if args.cublas_peak else None
     traffic = read_traffic()
-    tr_key = f"{args.workload}:{dom}"
-    if bound == "tensor":
-        roof = {"bound": "tensor", "achieved": algo_flops / dom_s / 1e12, "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": (algo_flops / dom_s / 1e12) / fp8_peak,
-                "traffic": (traffic or {}).get(tr_key),
-                "peak_source": f"{peak_src} bf16 burst {bf16:.1f} TFLOP/s x nominal FP8:BF16 ratio 2"}
-    else:
-        roof = {"bound": "hbm", "achieved": algo_bytes / dom_s / 1e9, "peak": hbm, "unit": "GB/s",
-                "frac": (algo_bytes / dom_s / 1e9) / hbm, "traffic": (traffic or {}).get(tr_key),
-                "peak_source": f"{peak_src} HBM copy bandwidth"}
-    roof["kernel"] = (f"fp8mm_kernel<BN={plans[dom].info()['block_n']}, "
-                      f"{'slow' if plans[dom].info()['slow'] else 'fast'}> ({probs[dom].name}, "
-                      f"{'fast' if probs[dom].fast_accum else 'slow'} accumulation)")
-    roof["roofline_time_us"] = t_roof * 1e6
-    roof["gbs"] = algo_bytes / dom_s / 1e9
-    roof["algorithmic_flops_per_launch"] = algo_flops
-    roof["algorithmic_bytes_per_launch"] = algo_bytes
-    per_call_ms = [1e3 * statistics.median(x) for x in per_call]
+    plans = [pm.plan_for((p.M, p.N, p.K, p.L, p.a_fmt, p.b_fmt, p.scale_mode, p.out_dtype,
+                          1 if p.fast_accum else 0, 0, 0, 0, local_rank, 0)) for _, _, p in probs]
+    launches = sum(pl.kernel_launches() for pl in plans)
+    per_config = []
+    for i, ((name, desc, p), pl) in enumerate(zip(probs, plans)):
+        f, by = pl.roofline()
+        med = statistics.median(per_call[i])
+        tensor_bound = f / (fp8_peak * 1e12) >= by / (hbm * 1e9)
+        tf, gbs = f / med / 1e12, by / med / 1e9
+        entry = {"name": name, "what": desc, "us": med * 1e6, "tflops": tf, "gbs": gbs,
+                 "bound": "tensor" if tensor_bound else "hbm",
+                 "frac": tf / fp8_peak if tensor_bound else gbs / hbm,
+                 "roofline_us": max(f / (fp8_peak * 1e12), by / (hbm * 1e9)) * 1e6,
+                 "plan": pl.info(), "traffic": traffic.get(name)}
+        if isinstance(cublas, float) and tensor_bound:
+            entry["frac_of_cublas_fp8"] = tf / cublas
+            entry["frac_of_nominal_fp8"] = tf / FP8_NOMINAL_TFLOPS
+        per_config.append(entry)
+    d = per_config[dom]
+    roof = {"bound": d["bound"], "achieved": d["tflops"] if d["bound"] == "tensor" else d["gbs"],
+            "peak": fp8_peak if d["bound"] == "tensor" else hbm,
+            "unit": "TFLOP/s" if d["bound"] == "tensor" else "GB/s", "frac": d["frac"], "traffic": d["traffic"],
+            "peak_source": (f"{peak_src} bf16 burst {bf16:.1f} TFLOP/s x nominal FP8:BF16 ratio 2"
+                            if d["bound"] == "tensor" else f"{peak_src} HBM copy bandwidth"),
+            "kernel": f"fp8mm_kernel ({d['name']}: BN={d['plan']['block_n']}, "
+                      f"{'CTA pair' if d['plan']['cta_pair'] else 'one CTA'}, "
+                      f"{'slow' if d['plan']['slow'] else 'fast'} accumulation)",
+            "algorithmic_flops_per_launch": plans[dom].roofline()[0],
+            "algorithmic_bytes_per_launch": plans[dom].roofline()[1],
+            "us_per_launch": d["us"], "roofline_time_us": d["roofline_us"]}
     cpu = None
     if not args.no_cpu_baseline:
         v, cores, sample = oracle_sample(probs, target_s=args.cpu_seconds)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
-    p0 = probs[0]
+    fmts = sorted({("fp8_e4m3" if p.a_fmt == 0 else "fp8_e5m2") for _, _, p in probs})
+    cfg = config_of(args.workload, probs)
+    cfg.update({"l2": "L2 flushed before every timed GEMM: 256 MiB written, then read back (not timed)",
+                "parallelism": f"replicas x{world}"})
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8_e4m3" if p0.a_fmt == 0 else "fp8_e5m2", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC.get(args.workload, args.workload), "M": p0.M, "N": p0.N,
-                       "K": p0.K, "L": p0.L, "calls_per_step": len(probs),
-                       "per_call_ms": per_call_ms, "plans": [pl.info() for pl in plans],
-                       "l2": "L2 flushed before every timed GEMM: 256 MiB written, then read back (not timed)",
-                       "parallelism": f"replicas x{world}"},
-            "roofline": roof, "cpu_baseline": cpu,
+            "vs_baseline": None, "dtype": "/".join(fmts) + " operands, fp32 accumulation", "data": "synthetic",
+            "config": cfg, "per_config": per_config, "roofline": roof,
+            "peaks": {"fp8_tflops_used": fp8_peak, "hbm_gbs_used": hbm, "source": peak_src,
+                      "fp8_nominal_dense_tflops": FP8_NOMINAL_TFLOPS, "cublas_fp8_8192cubed_tflops": cublas,
+                      "fp8_sustained_from_bf16_tflops": bf16_sus * FP8_PER_BF16},
+            "sustained": sustained, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches * args.steps, "clocks": clk.summary(), "wall_s": t_wall,
             "kernel_sources_sha256_16": kernel_hash()}
@@ -409,12 +526,14 @@ def run_ours(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llm_4096")
+    ap.add_argument("--workload", default="all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--sustain-s", type=float, default=2.0)
+    ap.add_argument("--no-cublas-peak", dest="cublas_peak", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

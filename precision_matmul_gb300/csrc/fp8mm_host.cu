@@ -125,7 +125,7 @@ size_t layout(fp8mm_plan_s* P, int stages) {
   off += (uint32_t)(P->ew * stage_out_bytes(P->ew, held_tile(P->bn, P->slow != 0, P->mx != 0)));
   P->off_ys = off;
   // per-column Y scales of the current chunk, one row per epilogue warp
-  if (P->x_kind != kScaleNone && P->y_kind == kScaleRow) off += (uint32_t)(P->ew * part_max_cols(P->bn, P->ew) * 4);
+  if (P->x_kind != kScaleNone && P->y_kind == kScaleRow) off += (uint32_t)(P->ew * part_max_cols(P->bn, P->ew, P->slow != 0) * 4);
   off = (off + 127u) & ~127u;
   P->off_bar = off;
   off += 16u * stages + 80u + 16u;  // full/empty per stage, 4+4 accumulator barriers, epilogue, drain, misc
@@ -250,10 +250,22 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   const bool auto_pair = d.cta_pair == 0 && !mx && !P->slow && !swap && P->Q > 128 &&
                          (d.block_n == 0 || d.block_n == 224 || d.block_n == 256) &&
                          pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
-  if (bn == 0 && auto_pair) {
+  // Slow accumulation on CTA pairs: 256-row tiles of 224 or 256 columns whose
+  // promoted sums stay in registers.  Each SM stages 128 rows of X and half of
+  // Y per 128-K step (32 KiB instead of the 48 KiB of a one-CTA 256-column
+  // tile), and operand staging from L2, not the promotion, is what bounds slow
+  // tiles on GB300.  A 224-column tile's halves (112 columns per epilogue
+  // warp) straddle 128-column scale blocks, so 128x128 Y scales take 256.
+  const bool y_block128 = blockwise && P->y_kind == kScaleBlock128;
+  const bool auto_slow_pair = d.cta_pair == 0 && !mx && P->slow && !swap && P->Q > 128 && d.splitk <= 1 &&
+                              (d.epi_warps == 0 || d.epi_warps == 8) &&
+                              (d.block_n == 0 || d.block_n == 256 || (d.block_n == 224 && !y_block128)) &&
+                              pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
+  if (bn == 0 && (auto_pair || auto_slow_pair)) {
     // the width whose whole waves over the SM pairs cost least
     double best = 1e300;
     for (int c : {256, 224}) {
+      if (auto_slow_pair && c == 224 && y_block128) continue;
       const int64_t tiles = pair_rows * cdiv(P->Q, c) * L;
       const double cost = (double)cdiv(tiles, P->sms / 2) * c / width_efficiency(c, false);
       if (cost < best * 0.999) {
@@ -288,12 +300,16 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
         }
       }
     }
-    // Slow accumulation keeps the promoted sums in registers: 256 columns
-    // only for the unswapped, unsplit single-CTA form.
-    if (P->slow && bn > 128 && (bn != 256 || swap || mx || d.cta_pair == 1 || d.splitk > 1)) bn = 128;
   }
-  if (P->slow && bn > 128 && (bn != 256 || swap || mx || d.cta_pair == 1 || d.splitk > 1))
-    return FP8MM_ERR_UNSUPPORTED;
+  // Slow accumulation keeps the promoted sums in registers: 256 columns on one
+  // CTA or a CTA pair, 224 on a CTA pair only, never swapped, split or MX.
+  const bool pair = d.cta_pair == 1 || auto_pair || auto_slow_pair;
+  const bool slow_wide_ok = !swap && !mx && d.splitk <= 1 &&
+                            (bn == 256 || (bn == 224 && pair && !y_block128));
+  if (P->slow && bn > 128 && !slow_wide_ok) {
+    if (d.block_n != 0) return FP8MM_ERR_UNSUPPORTED;
+    bn = 128;
+  }
   // (a requested split needs the narrower MX tile: 256-column ones are held)
   if (mx && !P->slow && bn == 256 && d.block_n == 0 && d.splitk > 1) bn = 128;
   // MX tiles are 128 or 256 columns, or 224: the block-scaled MMA reads its
@@ -302,7 +318,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   if (mx && bn != 128 && bn != 224 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
   P->bn = bn;
 
-  if (d.cta_pair == 1 || auto_pair) {
+  if (d.cta_pair == 1 || auto_pair || (auto_slow_pair && bn > 128)) {
     if (mx || swap) return FP8MM_ERR_UNSUPPORTED;
     P->cg = 2;
   }

@@ -69,8 +69,9 @@ static_assert(2 * epi_regs(8) + kRegRoles <= 512 && 4 * epi_regs(16) + kRegRoles
 static_assert((8 * epi_regs(8) + 4 * kRegRoles) <= 12 * launch_regs(8) &&
                   (16 * epi_regs(16) + 4 * kRegRoles) <= 20 * launch_regs(16),
               "register split within the launch's allocation");
-// Slow accumulation on 256-column tiles: each epilogue warp keeps 128 (8
-// warps) or 64 (16 warps) promoted fp32 sums per row in registers.
+// Slow accumulation on 224- and 256-column tiles: each epilogue warp keeps 112
+// or 128 (8 warps) or 64 (16 warps, 256 columns) promoted fp32 sums per row in
+// registers.
 __host__ __device__ constexpr bool wide_slow(int bn, bool slow) { return slow && bn > 128; }
 // Tiles whose epilogue holds the whole tile in registers before storing it:
 // slow 256-column tiles (the promoted sums) and MX 256-column tiles, whose
@@ -84,10 +85,16 @@ __host__ __device__ constexpr bool held_tile(int bn, bool slow, bool mx) {
 // less room).  (Rows of 16 B measured far slower: the stores then write half
 // sectors.)
 __host__ __device__ constexpr int stage_out_bytes(int ew, bool held) { return (ew == 8 && !held) ? 4096 : 2048; }
-// Columns [0, half0_cols) belong to epilogue warps 0-3, the rest to warps 4-7.
-__host__ __device__ constexpr int half0_cols(int bn) { return bn <= 64 ? bn / 2 : ((bn / 2 + 31) / 32) * 32; }
+// Columns [0, half0_cols) belong to epilogue warps 0-3, the rest to warps 4-7
+// (slow 224- and 256-column tiles split evenly: every warp promotes as many
+// columns as its neighbour).
+__host__ __device__ constexpr int half0_cols(int bn, bool slow = false) {
+  return (bn <= 64 || wide_slow(bn, slow)) ? bn / 2 : ((bn / 2 + 31) / 32) * 32;
+}
 // Widest column range of one epilogue warp.
-__host__ __device__ constexpr int part_max_cols(int bn, int ew) { return ew == 8 ? half0_cols(bn) : bn / 4; }
+__host__ __device__ constexpr int part_max_cols(int bn, int ew, bool slow = false) {
+  return ew == 8 ? half0_cols(bn, slow) : bn / 4;
+}
 // Columns of one output chunk (one TMA store of 32 tile rows).
 __host__ __device__ constexpr int chunk_cols(int bn, int es, int ew, bool held) {
   return held ? 32 / es
@@ -332,15 +339,14 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
                                          uint32_t tmem_base, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t bar_epi,
                                          volatile uint32_t* misc, volatile uint32_t* abort_flag, uint32_t rank,
                                          long long u_first, long long u_step, int warp, int lane) {
-  constexpr int HMAX = part_max_cols(BN, EW);  // widest column range of a warp
-  constexpr bool WIDE = wide_slow(BN, SLOW);     // slow 256-column tile: HMAX promoted sums per thread
+  constexpr int HMAX = part_max_cols(BN, EW, SLOW);  // widest column range of a warp
+  constexpr bool WIDE = wide_slow(BN, SLOW);  // slow 224/256-column tile: HMAX promoted sums per thread
   // columns per tcgen05.ld while promoting (held tiles: 16, measured faster than 8 or 32)
   constexpr int LDW = HMAX < 32 ? HMAX : (HOLD ? 16 : 32);
   static_assert(!WIDE || HOLD, "slow 256-column tiles hold their sums");
   static_assert(EW == 8 || EW == 16, "8 or 16 epilogue warps");
   static_assert(EW == 8 || BN % 128 == 0, "16 epilogue warps split 128-multiple tiles in four");
   static_assert(!SLOW || HMAX * (EW / 4) == BN, "slow accumulation splits the tile evenly");
-  static_assert(!HOLD || CG == 1, "held tiles run on one CTA");
   static_assert(HMAX % CW == 0 && (BN - HMAX) % CW == 0, "chunks tile each part");
   constexpr int kStageOut = stage_out_bytes(EW, HOLD);
   const int qd = warp & 3;
@@ -698,8 +704,8 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(!MX || BN == 128 || BN == 256 || (BN % 32 == 0 && BN < 256),
                 "MX tiles start on a 32-row boundary of a factor atom");
-  static_assert(!SLOW || BN <= 128 || (BN == 256 && CG == 1 && !MX),
-                "slow accumulation keeps its promoted sums in registers: 256-column tiles on one CTA");
+  static_assert(!SLOW || BN <= 128 || ((BN == 256 || BN == 224) && !MX && EW == 8) || (BN == 256 && CG == 1 && !MX),
+                "slow accumulation keeps its promoted sums in registers: 224- or 256-column tiles");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
   static_assert(!MX || CG == 1, "the block-scaled form runs on single-CTA tiles");
   extern __shared__ uint8_t smem_raw[];
@@ -718,8 +724,10 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
   if constexpr (held_tile(BN, SLOW, MX)) {
-    // Held tiles are planned without split-K or swapped operands.
-    if (p.splits != 1 || p.swap) {
+    // Held tiles are planned without split-K or swapped operands, and a
+    // 224-column tile (whose halves straddle 128-column blocks) without
+    // 128x128 Y scales.
+    if (p.splits != 1 || p.swap || (BN % 128 != 0 && p.y_kind == kScaleBlock128)) {
       if (threadIdx.x == 0) atomicOr(p.abort_word, kErrPlan);
       return;
     }

@@ -24,6 +24,8 @@ KernelFn kernel_bn128_slow_f8_cg1_ew8();
 KernelFn kernel_bn128_slow_f8_cg1_ew16();
 KernelFn kernel_bn256_slow_f8_cg1_ew8();
 KernelFn kernel_bn256_slow_f8_cg1_ew16();
+KernelFn kernel_bn256_slow_f8_cg2_ew8();
+KernelFn kernel_bn224_slow_f8_cg2_ew8();
 KernelFn kernel_bn128_fast_mx_cg1_ew8();
 KernelFn kernel_bn224_fast_mx_cg1_ew8();
 KernelFn kernel_bn256_fast_mx_cg1_ew8();
@@ -54,6 +56,8 @@ inline const KernelEntry* kernel_table(int* n) {
       {128, 1, 0, 1, 16, &kernel_bn128_slow_f8_cg1_ew16},
       {256, 1, 0, 1, 8, &kernel_bn256_slow_f8_cg1_ew8},
       {256, 1, 0, 1, 16, &kernel_bn256_slow_f8_cg1_ew16},
+      {256, 1, 0, 2, 8, &kernel_bn256_slow_f8_cg2_ew8},
+      {224, 1, 0, 2, 8, &kernel_bn224_slow_f8_cg2_ew8},
       {128, 0, 1, 1, 8, &kernel_bn128_fast_mx_cg1_ew8},
       {224, 0, 1, 1, 8, &kernel_bn224_fast_mx_cg1_ew8},
       {256, 0, 1, 1, 8, &kernel_bn256_fast_mx_cg1_ew8},
