@@ -20,11 +20,23 @@
  *     fp32 = max |C|; A, B, C 16-byte aligned along the contiguous dimension;
  *     A and B of the same dtype for the block-scaled form.
  *
+ *   - TileOPs "Linear Algebra Operators", GemmFP8FwdOp: an optional bias [N]
+ *     in out_dtype, d = (a s_a) @ (b s_b)^T + bias; GemmFwdOp's layout table
+ *     (NT, NN, TN, TT); BmmFP8FwdOp: a b that is not K-innermost is copied
+ *     into a K-major buffer first (one extra read and write of it).
+ *   - mmaemu "API reference (v0.1)", mmaemu.scaled_mm: out_dtype may also be
+ *     float8_e4m3fn or float8_e5m2, and scale_result (one fp32) is used only
+ *     for those FP8 outputs.
+ *
  * Memory layout (all row-major, batch outermost):
- *   a        [L][M][K] FP8 codes (1 byte each), K contiguous.
- *   b        [L][N][K] FP8 codes, K contiguous.
+ *   a        [L][M][K] FP8 codes (1 byte each), K contiguous (a_major = 0), or
+ *            [L][K][M], M contiguous (a_major = 1: the "T" of TN / TT).
+ *   b        [L][N][K] FP8 codes, K contiguous (b_major = 0), or [L][K][N], N
+ *            contiguous (b_major = 1: the "N" of NN / TN).
  *   c        [L][M][N] of out_dtype, N contiguous.
  *   amax     one fp32.
+ *   bias     [N] of out_dtype (fp32, bf16 or fp16 outputs only), when desc.bias = 1.
+ *   scale_result  one fp32 (FP8 outputs; NULL means 1).
  *   scale_a / scale_b, by scale_mode:
  *     FP8MM_SCALE_TENSOR           one fp32 each.
  *     FP8MM_SCALE_A1x128_B1x128    fp32 [L][M][ceil(K/128)] and [L][N][ceil(K/128)].
@@ -61,7 +73,17 @@ extern "C" {
 
 typedef enum { FP8MM_E4M3 = 0, FP8MM_E5M2 = 1 } fp8mm_fmt;
 
-typedef enum { FP8MM_OUT_F32 = 0, FP8MM_OUT_BF16 = 1, FP8MM_OUT_F16 = 2 } fp8mm_out;
+/* FP8 outputs (E4M3, E5M2): C = round_sat(fp32(alpha * acc) * scale_result), rounded once to
+ * nearest even and saturated to the largest finite value (NaN stays NaN); amax is then
+ * max |fp32(alpha * acc)|, before scale_result and the rounding (it sets the next quantisation
+ * scale).  FP8 outputs need N % 16 == 0 and take no bias. */
+typedef enum {
+  FP8MM_OUT_F32 = 0,
+  FP8MM_OUT_BF16 = 1,
+  FP8MM_OUT_F16 = 2,
+  FP8MM_OUT_E4M3 = 3,
+  FP8MM_OUT_E5M2 = 4
+} fp8mm_out;
 
 typedef enum {
   FP8MM_SCALE_TENSOR = 0,
@@ -102,8 +124,15 @@ typedef struct {
   int32_t epi_warps;   /* epilogue warps per CTA: 0 choose, 8 or 16 */
   int32_t stages;      /* shared-memory pipeline depth: 0 choose (as many as fit), else 2..12 */
   int32_t strict_torch; /* 0: accept all four E4M3/E5M2 pairs; 1: refuse with FP8MM_ERR_REJECTED
-                           the pair torch._scaled_mm refuses, E5M2 x E5M2 (mmaemu "Testing
-                           mmaemu", T1 hw_mini, expected error classes) */
+                           what torch._scaled_mm refuses: E5M2 x E5M2, and E4M3 x E4M3 with an
+                           E5M2 output (mmaemu "Testing mmaemu", T1 hw_mini, expected error
+                           classes) */
+  int32_t bias;        /* 1: fp8mm_run_ex adds bias[n] (out_dtype, N values) to every row before the
+                          one rounding (TileOPs GemmFP8FwdOp); not for FP8 outputs.  0: no bias. */
+  int32_t a_major;     /* 0: a is [L][M][K] (K-major); 1: a is [L][K][M] (M-major, M % 16 == 0) */
+  int32_t b_major;     /* 0: b is [L][N][K] (K-major); 1: b is [L][K][N] (N-major, N % 16 == 0).
+                          An M/N-major operand is copied into K-major workspace by one extra
+                          HBM-bound kernel before the GEMM (BmmFP8FwdOp's transposing copy). */
 } fp8mm_desc;
 
 typedef struct fp8mm_plan_s fp8mm_plan_t;
@@ -123,26 +152,49 @@ typedef struct {
   int32_t epi_warps;    /* epilogue warps per CTA */
 } fp8mm_plan_info;
 
-/* Validate desc and choose tiles, swap-AB and split-K for the device.  On
+/* Validate desc and choose tiles, swap-AB and split-K for the device (the
+ * check-support-then-compile step of cuDNN "GEMM + Amax (SM100)", Class API:
+ * everything that can be refused is refused here, before any call).  On
  * success *out owns a new plan (free with fp8mm_destroy).  Reads the device's
- * SM count; launches nothing. */
+ * SM count and kernel attributes; launches nothing.  Errors: INVALID (null
+ * pointer, negative size, field out of range), ALIGNMENT (K % 16, rows of C
+ * not 16-byte multiples, an M/N-major operand with M or N % 16), UNSUPPORTED
+ * (a form or override this library does not build), REJECTED (strict_torch),
+ * CUDA (a device query failed). */
 fp8mm_status fp8mm_plan(const fp8mm_desc* desc, fp8mm_plan_t** out);
 
-/* Device bytes the caller must pass as workspace to fp8mm_run (0 if none).
- * The split-K partial tiles and their arrival counters live there. */
+/* Device bytes the caller must pass as workspace to fp8mm_run (0 if none):
+ * the K-major copies of M/N-major operands, then the split-K partial tiles
+ * and their arrival counters (the workspace a profile states up front in
+ * mmaemu "API reference (v0.1)", Profile; here the caller allocates it). */
 fp8mm_status fp8mm_workspace_size(const fp8mm_plan_t* plan, size_t* bytes);
 
 /* Enqueue one GEMM + amax on `stream` (a cudaStream_t; NULL = legacy default
- * stream).  a, b, scale_a, scale_b, c, amax, workspace: device pointers laid
- * out as described above.  a, b and c must be 16-byte aligned; scale pointers
- * 4-byte aligned (MX factor atoms 16-byte aligned), workspace 256-byte
- * aligned; else FP8MM_ERR_ALIGNMENT.  c and amax are written, never read. */
+ * stream): torch._scaled_mm's product (mmaemu "API reference (v0.1)",
+ * mmaemu.scaled_mm) with TileOPs GemmFP8FwdOp's scale forms and cuDNN "GEMM +
+ * Amax (SM100)"'s block-scaled form and Amax.  a, b, scale_a, scale_b, c,
+ * amax, workspace: device pointers laid out as described above.  a, b and c
+ * must be 16-byte aligned; scale pointers 4-byte aligned (MX factor atoms
+ * 16-byte aligned), workspace 256-byte aligned; else FP8MM_ERR_ALIGNMENT.
+ * c and amax are written, never read.  Plans with desc.bias = 1 must use
+ * fp8mm_run_ex (FP8MM_ERR_INVALID here); FP8 outputs get scale_result = 1. */
 fp8mm_status fp8mm_run(fp8mm_plan_t* plan, const void* a, const void* b, const void* scale_a,
                        const void* scale_b, void* c, float* amax, void* workspace,
                        size_t workspace_bytes, void* stream);
 
-/* Algorithmic work of one call: flops = 2*M*N*K*L; bytes = A + B + scales +
- * C + amax (split-K workspace traffic not counted). */
+/* fp8mm_run with the two epilogue operands: scale_result (device, one fp32,
+ * read only for FP8 outputs; NULL means 1) and bias (device, [N] of
+ * out_dtype, 4-byte aligned for fp32, 2-byte for bf16/fp16; required exactly
+ * when desc.bias = 1, else FP8MM_ERR_INVALID).  Sources: mmaemu.scaled_mm's
+ * scale_result; TileOPs GemmFP8FwdOp's bias. */
+fp8mm_status fp8mm_run_ex(fp8mm_plan_t* plan, const void* a, const void* b, const void* scale_a,
+                          const void* scale_b, const float* scale_result, const void* bias, void* c,
+                          float* amax, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Algorithmic work of one call (TileOPs "Linear Algebra Operators",
+ * eval_roofline: the flops and bytes the op must do at least): flops =
+ * 2*M*N*K*L; bytes = A + B + scales + bias + C + amax (workspace traffic --
+ * split-K partials and K-major copies of M/N-major operands -- not counted). */
 fp8mm_status fp8mm_plan_roofline(const fp8mm_plan_t* plan, double* flops, double* bytes);
 
 fp8mm_status fp8mm_plan_get_info(const fp8mm_plan_t* plan, fp8mm_plan_info* info);
@@ -186,7 +238,11 @@ fp8mm_status fp8mm_plan_kernel_launches(const fp8mm_plan_t* plan, int32_t* launc
  *     is rejected with FP8MM_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on a device that needs scratch looks up the array's
  *     device address (cudaGetSymbolAddress, with that device current); make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The address is kept for
+ *     the life of the process, so it assumes the device's primary context is
+ *     not reset (cudaDeviceReset) in between.
+ *   - Plans with M/N-major operands need workspace for their K-major copies
+ *     too; it counts against the same limit.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents.  Each call resets the parts that must start at zero on its
  *     stream, so calls in stream order are independent; calls that may run

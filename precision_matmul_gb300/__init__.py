@@ -20,14 +20,15 @@ from __future__ import annotations
 import threading
 
 from . import _binding
-from ._binding import (FP8MM_E4M3, FP8MM_E5M2, FP8MM_OUT_BF16, FP8MM_OUT_F16, FP8MM_OUT_F32,
-                       FP8MM_SCALE_A1x128_B1x128, FP8MM_SCALE_A1x128_B128x128, FP8MM_SCALE_MX32_UE8M0,
-                       FP8MM_SCALE_TENSOR, FP8MMError, Plan, fp8mm_device_error, fp8mm_gemm, fp8mm_plan,
-                       fp8mm_run, fp8mm_status_string, make_desc)
+from ._binding import (FP8MM_E4M3, FP8MM_E5M2, FP8MM_OUT_BF16, FP8MM_OUT_E4M3, FP8MM_OUT_E5M2, FP8MM_OUT_F16,
+                       FP8MM_OUT_F32, FP8MM_SCALE_A1x128_B1x128, FP8MM_SCALE_A1x128_B128x128,
+                       FP8MM_SCALE_MX32_UE8M0, FP8MM_SCALE_TENSOR, FP8MMError, Plan, fp8mm_device_error,
+                       fp8mm_gemm, fp8mm_plan, fp8mm_run, fp8mm_run_ex, fp8mm_status_string, make_desc)
 
-__all__ = ["scaled_mm", "torch_scaled_mm", "bmm_fp8", "describe", "plan_for", "Plan", "FP8MMError", "fp8mm_plan", "fp8mm_run", "fp8mm_gemm",
+__all__ = ["scaled_mm", "torch_scaled_mm", "bmm_fp8", "describe", "operand_majors", "plan_for", "Plan", "FP8MMError",
+           "fp8mm_plan", "fp8mm_run", "fp8mm_run_ex", "fp8mm_gemm",
            "fp8mm_device_error", "fp8mm_status_string", "make_desc", "FP8MM_E4M3", "FP8MM_E5M2",
-           "FP8MM_OUT_F32", "FP8MM_OUT_BF16", "FP8MM_OUT_F16", "FP8MM_SCALE_TENSOR",
+           "FP8MM_OUT_F32", "FP8MM_OUT_BF16", "FP8MM_OUT_F16", "FP8MM_OUT_E4M3", "FP8MM_OUT_E5M2", "FP8MM_SCALE_TENSOR",
            "FP8MM_SCALE_A1x128_B1x128", "FP8MM_SCALE_A1x128_B128x128", "FP8MM_SCALE_MX32_UE8M0"]
 
 _lock = threading.Lock()
@@ -58,10 +59,28 @@ def _fmt_of(t, explicit):
 
 def _out_code(dtype):
     torch = _torch()
-    table = {torch.float32: FP8MM_OUT_F32, torch.bfloat16: FP8MM_OUT_BF16, torch.float16: FP8MM_OUT_F16}
+    table = {torch.float32: FP8MM_OUT_F32, torch.bfloat16: FP8MM_OUT_BF16, torch.float16: FP8MM_OUT_F16,
+             torch.float8_e4m3fn: FP8MM_OUT_E4M3, torch.float8_e5m2: FP8MM_OUT_E5M2}
     if dtype not in table:
-        raise TypeError(f"out_dtype {dtype}: float32, bfloat16 or float16")
+        raise TypeError(f"out_dtype {dtype}: float32, bfloat16, float16, float8_e4m3fn or float8_e5m2")
     return table[dtype]
+
+
+def _major(t, name):
+    """0 if t ([.., rows, K]) has K contiguous; 1 if it is the transposed view
+    of a contiguous [.., K, rows] tensor (rows contiguous)."""
+    if t.is_contiguous():
+        return 0
+    if t.transpose(-1, -2).is_contiguous():
+        return 1
+    raise ValueError(f"{name} must be contiguous along K, or the transpose of a tensor contiguous along its rows")
+
+
+def operand_majors(a, b):
+    """(a_major, b_major) of fp8mm_desc from the operands' strides: a [.., M, K]
+    and b [.., N, K] views are K-major when K is contiguous, M/N-major when
+    they are transposed views of tensors stored [.., K, M] / [.., K, N]."""
+    return _major(a, "a"), _major(b, "b")
 
 
 def _mx_dtypes():
@@ -98,7 +117,7 @@ def _infer_scale_mode(scale_a, scale_b, L, M, N, K):
 
 
 def describe(a, b, scale_a, scale_b, *, out_dtype=None, a_fmt=None, b_fmt=None, scale_mode=None, out=None,
-             amax=None):
+             amax=None, bias=None, scale_result=None):
     """Check the arguments of ``scaled_mm`` on the host and return
     ``(L, M, N, K, a_fmt, b_fmt, scale_mode, out_code, out_shape)``.
 
@@ -106,7 +125,10 @@ def describe(a, b, scale_a, scale_b, *, out_dtype=None, a_fmt=None, b_fmt=None, 
     ABI only sees pointers: operand formats, that every tensor sits on one
     device and is contiguous, and that the scale tensors hold exactly the
     elements their form reads (a short scale tensor would be read past its
-    end on the device).  Raises TypeError or ValueError."""
+    end on the device).  a and b may also be transposed views of tensors
+    stored K-outermost (``operand_majors``); their rows must then be 16-byte
+    multiples.  A bias is [N] of out_dtype (not for FP8 outputs);
+    scale_result is one fp32 (FP8 outputs).  Raises TypeError or ValueError."""
     torch = _torch()
     if out_dtype is None:
         out_dtype = torch.bfloat16
@@ -118,11 +140,14 @@ def describe(a, b, scale_a, scale_b, *, out_dtype=None, a_fmt=None, b_fmt=None, 
     N = b.shape[-2]
     if b.shape[-1] != K or (batched and b.shape[0] != L):
         raise ValueError("a and b disagree on K or L")
-    tensors = [a, b, scale_a, scale_b] + [t for t in (out, amax) if t is not None]
-    if any(t.device != a.device for t in tensors):
+    others = [scale_a, scale_b] + [t for t in (out, amax, bias, scale_result) if t is not None]
+    if any(t.device != a.device for t in [a, b] + others):
         raise ValueError("all tensors must be on one device")
-    if not all(t.is_contiguous() for t in tensors):
-        raise ValueError("a, b, the scales, out and amax must be contiguous (K innermost for a and b)")
+    if not all(t.is_contiguous() for t in others):
+        raise ValueError("the scales, out, amax and bias must be contiguous")
+    am, bm = operand_majors(a, b)
+    if (am and M % 16) or (bm and N % 16):
+        raise ValueError("a K-outermost operand needs rows (M or N) that are multiples of 16")
     fa, fb = _fmt_of(a, a_fmt), _fmt_of(b, b_fmt)
     oc = _out_code(out_dtype)
     mode = int(scale_mode) if scale_mode is not None else _infer_scale_mode(scale_a, scale_b, L, M, N, K)
@@ -142,16 +167,24 @@ def describe(a, b, scale_a, scale_b, *, out_dtype=None, a_fmt=None, b_fmt=None, 
         raise ValueError("out has the wrong shape or dtype")
     if amax is not None and (amax.dtype != torch.float32 or amax.numel() < 1):
         raise ValueError("amax must hold at least one float32")
+    if bias is not None:
+        if oc in (FP8MM_OUT_E4M3, FP8MM_OUT_E5M2):
+            raise ValueError("a bias is not defined for FP8 outputs")
+        if bias.dtype != out_dtype or bias.numel() != N:
+            raise ValueError("bias must hold N values of out_dtype")
+    if scale_result is not None and (scale_result.dtype != torch.float32 or scale_result.numel() != 1):
+        raise ValueError("scale_result must be one float32")
     return L, M, N, K, fa, fb, mode, oc, shape
 
 
-_KEY_LEN = 16
+_KEY_LEN = 19
 
 
 def normalize_key(desc_key: tuple) -> tuple:
     """The canonical plan key: (M, N, K, L, a_fmt, b_fmt, scale_mode, out_dtype,
     fast_accum, splitk, swap_ab, block_n, device, cta_pair, epi_warps,
-    strict_torch), with fields left off the end taken as 0."""
+    strict_torch, bias, a_major, b_major), with fields left off the end taken
+    as 0."""
     key = tuple(int(x) for x in desc_key)
     if not 13 <= len(key) <= _KEY_LEN:
         raise ValueError(f"plan key of {len(key)} fields")
@@ -166,7 +199,7 @@ def plan_for(desc_key: tuple) -> Plan:
         if p is None:
             p = Plan(make_desc(*k[:4], a_fmt=k[4], b_fmt=k[5], scale_mode=k[6], out_dtype=k[7], fast_accum=k[8],
                                splitk=k[9], swap_ab=k[10], block_n=k[11], device=k[12], cta_pair=k[13],
-                               epi_warps=k[14], strict_torch=k[15]))
+                               epi_warps=k[14], strict_torch=k[15], bias=k[16], a_major=k[17], b_major=k[18]))
             _plans[k] = p
         return p
 
@@ -186,20 +219,27 @@ def _workspace(device, stream_handle, nbytes):
 
 def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a_fmt=None, b_fmt=None,
               scale_mode=None, out=None, amax=None, splitk=0, swap_ab=0, block_n=0, cta_pair=0, epi_warps=0,
-              strict_torch=False):
-    """C = (a * scale_a) @ (b * scale_b)^T and amax = max |C|, on a's CUDA device.
+              strict_torch=False, bias=None, scale_result=None):
+    """C = (a * scale_a) @ (b * scale_b)^T (+ bias) and amax = max |C|, on a's CUDA device.
 
-    a: [M, K] or [L, M, K]; b: [N, K] or [L, N, K]; both K-contiguous FP8
-    (float8_e4m3fn / float8_e5m2, or uint8 codes with a_fmt / b_fmt).
-    Scales are device tensors: fp32 one-element (per-tensor), fp32 1x128 /
-    128x128 block scales, or uint8 / float8_e8m0fnu MX factor atoms.
-    Returns (C, amax) with C of out_dtype (default bfloat16) and amax a
-    one-element fp32 tensor.  splitk, swap_ab, block_n, cta_pair and
-    epi_warps override the planner's choices (0 leaves them to it; meanings as
-    in fp8mm_desc).  strict_torch=True refuses (FP8MMError, FP8MM_ERR_REJECTED)
-    the format pair torch._scaled_mm refuses, E5M2 x E5M2.  Enqueued on the current stream; nothing is
-    synchronised.  One workspace per (device, stream) is reused, so calls on
-    one stream must not overlap with calls of another thread on that stream.
+    a: [M, K] or [L, M, K]; b: [N, K] or [L, N, K]; FP8 (float8_e4m3fn /
+    float8_e5m2, or uint8 codes with a_fmt / b_fmt), each either K-contiguous
+    or the transposed view of a tensor stored K-outermost ([.., K, M] /
+    [.., K, N]: the NN / TN / TT layouts, copied into K-major workspace by the
+    library before the GEMM).  Scales are device tensors: fp32 one-element
+    (per-tensor), fp32 1x128 / 128x128 block scales, or uint8 / float8_e8m0fnu
+    MX factor atoms.  out_dtype (default bfloat16) may be float32, bfloat16,
+    float16, float8_e4m3fn or float8_e5m2; FP8 outputs are multiplied by
+    scale_result (one fp32 device tensor, default 1) before their saturating
+    rounding, and their amax is max |C| before scale_result.  bias: [N] of
+    out_dtype added to every row (not for FP8 outputs).
+    Returns (C, amax) with amax a one-element fp32 tensor.  splitk, swap_ab,
+    block_n, cta_pair and epi_warps override the planner's choices (0 leaves
+    them to it; meanings as in fp8mm_desc).  strict_torch=True refuses
+    (FP8MMError, FP8MM_ERR_REJECTED) what torch._scaled_mm refuses.  Enqueued
+    on the current stream; nothing is synchronised.  One workspace per
+    (device, stream) is reused, so calls on one stream must not overlap with
+    calls of another thread on that stream.
     """
     torch = _torch()
     if out_dtype is None:
@@ -207,11 +247,13 @@ def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a
     if not a.is_cuda:
         raise ValueError("all inputs must be CUDA tensors")
     L, M, N, K, fa, fb, mode, oc, shape = describe(a, b, scale_a, scale_b, out_dtype=out_dtype, a_fmt=a_fmt,
-                                                   b_fmt=b_fmt, scale_mode=scale_mode, out=out, amax=amax)
+                                                   b_fmt=b_fmt, scale_mode=scale_mode, out=out, amax=amax,
+                                                   bias=bias, scale_result=scale_result)
+    am, bm = operand_majors(a, b)
     device = a.device.index if a.device.index is not None else torch.cuda.current_device()
     fast = 1 if use_fast_accum else 0
     key = (M, N, K, L, fa, fb, int(mode), oc, fast, int(splitk), int(swap_ab), int(block_n), device, int(cta_pair),
-           int(epi_warps), int(bool(strict_torch)))
+           int(epi_warps), int(bool(strict_torch)), 1 if bias is not None else 0, am, bm)
     plan = plan_for(key)
     if out is None:
         out = torch.empty(shape, dtype=out_dtype, device=a.device)
@@ -220,8 +262,15 @@ def scaled_mm(a, b, scale_a, scale_b, *, out_dtype=None, use_fast_accum=False, a
     stream = torch.cuda.current_stream(a.device).cuda_stream
     nbytes = plan.workspace_size()
     ws = _workspace(device, stream, nbytes)
-    plan.run(a.data_ptr(), b.data_ptr(), scale_a.data_ptr(), scale_b.data_ptr(), out.data_ptr(),
-             amax.data_ptr(), ws.data_ptr() if ws is not None else None, nbytes, stream)
+    ws_ptr = ws.data_ptr() if ws is not None else None
+    if bias is None and scale_result is None:
+        plan.run(a.data_ptr(), b.data_ptr(), scale_a.data_ptr(), scale_b.data_ptr(), out.data_ptr(),
+                 amax.data_ptr(), ws_ptr, nbytes, stream)
+    else:
+        plan.run_ex(a.data_ptr(), b.data_ptr(), scale_a.data_ptr(), scale_b.data_ptr(),
+                    scale_result.data_ptr() if scale_result is not None else None,
+                    bias.data_ptr() if bias is not None else None, out.data_ptr(), amax.data_ptr(), ws_ptr, nbytes,
+                    stream)
     return out, amax
 
 
@@ -232,33 +281,36 @@ def torch_scaled_mm(input, mat2, scale_a, scale_b, bias=None, scale_result=None,
 
     input [M, K] row-major FP8; mat2 [K, N] FP8 in column-major storage (the
     ``w.t()`` of a row-major [N, K] weight); scale_a, scale_b one-element fp32
-    tensors that multiply the result; out_dtype defaults to input's dtype.
-    Returns the [M, N] result (use ``scaled_mm`` for the fused amax as well).
+    tensors that multiply the result; bias [N] of out_dtype; scale_result a
+    one-element fp32 tensor, read only for FP8 outputs; out_dtype defaults to
+    input's dtype and may be float32, bfloat16, float16, float8_e4m3fn or
+    float8_e5m2.  Returns the [M, N] result (use ``scaled_mm`` for the fused
+    amax as well).
 
-    As in torch, E5M2 x E5M2 is refused (FP8MMError with FP8MM_ERR_REJECTED).
-    Outside this library, raising NotImplementedError: a bias, FP8 outputs
-    (scale_result is read only for those, so it is ignored otherwise), and
-    row-wise scales.  mat2 in row-major storage raises ValueError: the kernels
-    read both operands K-contiguous.
+    As in torch, E5M2 x E5M2 and E4M3 x E4M3 -> E5M2 are refused (FP8MMError
+    with FP8MM_ERR_REJECTED), as are row-major mat2 (ValueError) and a bias
+    with an FP8 output (ValueError).  Row-wise scales raise NotImplementedError.
     """
     torch = _torch()
-    if bias is not None:
-        raise NotImplementedError("bias is not supported")
     if out_dtype is None:
         out_dtype = input.dtype
-    if out_dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
-        raise NotImplementedError("FP8 outputs are not supported; pass out_dtype float32, bfloat16 or float16")
     if input.dim() != 2 or mat2.dim() != 2:
         raise ValueError("input must be [M, K] and mat2 [K, N]")
     if mat2.shape[0] != input.shape[1]:
         raise ValueError("input and mat2 disagree on K")
     if scale_a.numel() != 1 or scale_b.numel() != 1:
         raise NotImplementedError("only tensor-wise (one-element) scales")
+    if not input.is_contiguous():
+        raise ValueError("input must be row-major ([M, K] with K contiguous)")
     b = mat2.t()  # [N, K]
     if not b.is_contiguous():
         raise ValueError("mat2 must be column-major ([K, N] with K contiguous, e.g. w.t() of a row-major weight)")
-    c, _ = scaled_mm(input, b, scale_a, scale_b, out_dtype=out_dtype, use_fast_accum=use_fast_accum,
-                     scale_mode=FP8MM_SCALE_TENSOR, out=out, strict_torch=True)
+    fp8_out = out_dtype in (torch.float8_e4m3fn, torch.float8_e5m2)
+    if scale_result is not None and not fp8_out:
+        scale_result = None  # read only for FP8 outputs
+    c, _ = scaled_mm(input, b, scale_a.reshape(1), scale_b.reshape(1), out_dtype=out_dtype,
+                     use_fast_accum=use_fast_accum, scale_mode=FP8MM_SCALE_TENSOR, out=out, strict_torch=True,
+                     bias=bias, scale_result=scale_result.reshape(1) if scale_result is not None else None)
     return c
 
 
@@ -268,12 +320,12 @@ def bmm_fp8(a, b, scale_a, scale_b, *, trans_b=False, out_dtype=None, use_fast_a
 
     a is [B, M, K]; b is [B, K, N] (trans_b False, torch.bmm's order) or
     [B, N, K] (trans_b True); scale_a and scale_b are per-tensor fp32 (0-dim or
-    one element); out_dtype defaults to bfloat16.  Whether b can be read in
-    place is decided by its strides, not by trans_b: the kernels read b with K
-    innermost, so a b whose [B, N, K] view is contiguous (a [B, N, K] tensor,
-    or the transpose of one given as [B, K, N]) is passed on without a copy.
-    Any other b raises ValueError (a transposing copy is not provided).
-    Returns d, [B, M, N] (use ``scaled_mm`` for the fused amax as well).
+    one element); out_dtype defaults to bfloat16.  As on that page, b's
+    strides, not trans_b, decide whether b is read in place: a b whose K axis
+    is innermost goes to the GEMM as it is; a b stored [B, K, N] with N
+    innermost is first copied into a K-major buffer by the library's
+    transposing kernel (one extra read and write of b).  Other strides raise
+    ValueError.  Returns d, [B, M, N] (use ``scaled_mm`` for the fused amax).
     """
     torch = _torch()
     if out_dtype is None:
@@ -283,8 +335,6 @@ def bmm_fp8(a, b, scale_a, scale_b, *, trans_b=False, out_dtype=None, use_fast_a
     bnk = b if trans_b else b.transpose(1, 2)
     if bnk.shape[0] != a.shape[0] or bnk.shape[2] != a.shape[2]:
         raise ValueError("a and b disagree on the batch or on K")
-    if not bnk.is_contiguous():
-        raise ValueError("b is not K-innermost; a transposing copy is not provided")
     d, _ = scaled_mm(a, bnk, scale_a.reshape(1), scale_b.reshape(1), out_dtype=out_dtype,
                      use_fast_accum=use_fast_accum, scale_mode=FP8MM_SCALE_TENSOR, out=out)
     return d

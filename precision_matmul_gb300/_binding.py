@@ -13,7 +13,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfp8mm.so")
 
 FP8MM_E4M3, FP8MM_E5M2 = 0, 1
-FP8MM_OUT_F32, FP8MM_OUT_BF16, FP8MM_OUT_F16 = 0, 1, 2
+FP8MM_OUT_F32, FP8MM_OUT_BF16, FP8MM_OUT_F16, FP8MM_OUT_E4M3, FP8MM_OUT_E5M2 = 0, 1, 2, 3, 4
 (FP8MM_SCALE_TENSOR, FP8MM_SCALE_A1x128_B1x128, FP8MM_SCALE_A1x128_B128x128,
  FP8MM_SCALE_MX32_UE8M0) = 0, 1, 2, 3
 STATUS = {0: "FP8MM_OK", 1: "FP8MM_ERR_INVALID", 2: "FP8MM_ERR_ALIGNMENT", 3: "FP8MM_ERR_UNSUPPORTED",
@@ -24,7 +24,8 @@ FP8MM_ERR_REJECTED, FP8MM_ERR_WORKSPACE, FP8MM_ERR_CUDA, FP8MM_ERR_DEVICE = 4, 5
 # Every symbol include/fp8mm.h declares.
 EXPORTS = ("fp8mm_plan", "fp8mm_workspace_size", "fp8mm_run", "fp8mm_plan_roofline",
            "fp8mm_plan_get_info", "fp8mm_destroy", "fp8mm_status_string", "fp8mm_device_error",
-           "fp8mm_plan_kernel_launches", "fp8mm_gemm", "fp8mm_run_static_workspace", "fp8mm_plan_preview")
+           "fp8mm_plan_kernel_launches", "fp8mm_gemm", "fp8mm_run_static_workspace", "fp8mm_plan_preview",
+           "fp8mm_run_ex")
 FP8MM_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 
@@ -34,7 +35,8 @@ class fp8mm_desc(ctypes.Structure):
                 ("out_dtype", ctypes.c_int32), ("fast_accum", ctypes.c_int32), ("splitk", ctypes.c_int32),
                 ("swap_ab", ctypes.c_int32), ("block_n", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("cta_pair", ctypes.c_int32), ("epi_warps", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("strict_torch", ctypes.c_int32)]
+                ("strict_torch", ctypes.c_int32), ("bias", ctypes.c_int32), ("a_major", ctypes.c_int32),
+                ("b_major", ctypes.c_int32)]
 
 
 class fp8mm_plan_info(ctypes.Structure):
@@ -87,6 +89,8 @@ def load():
     lib.fp8mm_run_static_workspace.restype = i32
     lib.fp8mm_plan_preview.argtypes = [ctypes.POINTER(fp8mm_desc), i32, i32, ctypes.POINTER(fp8mm_plan_info)]
     lib.fp8mm_plan_preview.restype = i32
+    lib.fp8mm_run_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.fp8mm_run_ex.restype = i32
     _lib = lib
     return lib
 
@@ -102,7 +106,7 @@ def _check(st: int, where: str):
 
 def make_desc(M, N, K, L=1, *, a_fmt=FP8MM_E4M3, b_fmt=FP8MM_E4M3, scale_mode=FP8MM_SCALE_TENSOR,
               out_dtype=FP8MM_OUT_BF16, fast_accum=1, splitk=0, swap_ab=0, block_n=0, device=0,
-              cta_pair=0, epi_warps=0, stages=0, strict_torch=0) -> fp8mm_desc:
+              cta_pair=0, epi_warps=0, stages=0, strict_torch=0, bias=0, a_major=0, b_major=0) -> fp8mm_desc:
     d = fp8mm_desc()
     d.M, d.N, d.K, d.L = int(M), int(N), int(K), int(L)
     d.a_fmt, d.b_fmt, d.scale_mode, d.out_dtype = int(a_fmt), int(b_fmt), int(scale_mode), int(out_dtype)
@@ -112,6 +116,7 @@ def make_desc(M, N, K, L=1, *, a_fmt=FP8MM_E4M3, b_fmt=FP8MM_E4M3, scale_mode=FP
     d.epi_warps = int(epi_warps)
     d.stages = int(stages)
     d.strict_torch = int(strict_torch)
+    d.bias, d.a_major, d.b_major = int(bias), int(a_major), int(b_major)
     return d
 
 
@@ -152,6 +157,12 @@ class Plan:
                               ctypes.c_size_t(int(ws_bytes)), stream)
         _check(st, "fp8mm_run")
 
+    def run_ex(self, a_ptr, b_ptr, sa_ptr, sb_ptr, sr_ptr, bias_ptr, c_ptr, amax_ptr, ws_ptr, ws_bytes,
+               stream) -> None:
+        st = load().fp8mm_run_ex(self._h, a_ptr, b_ptr, sa_ptr, sb_ptr, sr_ptr, bias_ptr, c_ptr, amax_ptr, ws_ptr,
+                                 ctypes.c_size_t(int(ws_bytes)), stream)
+        _check(st, "fp8mm_run_ex")
+
     def __del__(self):
         h = getattr(self, "_h", None)
         if h is not None and h.value and _lib is not None:
@@ -166,6 +177,11 @@ def fp8mm_plan(desc: fp8mm_desc) -> Plan:
 def fp8mm_run(plan: Plan, a_ptr, b_ptr, sa_ptr, sb_ptr, c_ptr, amax_ptr, ws_ptr=None, ws_bytes=0,
               stream=None) -> None:
     plan.run(a_ptr, b_ptr, sa_ptr, sb_ptr, c_ptr, amax_ptr, ws_ptr, ws_bytes, stream)
+
+
+def fp8mm_run_ex(plan: Plan, a_ptr, b_ptr, sa_ptr, sb_ptr, sr_ptr, bias_ptr, c_ptr, amax_ptr, ws_ptr=None,
+                 ws_bytes=0, stream=None) -> None:
+    plan.run_ex(a_ptr, b_ptr, sa_ptr, sb_ptr, sr_ptr, bias_ptr, c_ptr, amax_ptr, ws_ptr, ws_bytes, stream)
 
 
 def fp8mm_device_error(device: int = 0, clear: bool = True) -> int:

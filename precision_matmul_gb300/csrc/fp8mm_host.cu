@@ -34,6 +34,9 @@ struct fp8mm_plan_s {
   uint32_t x_stage_bytes = 0, y_stage_bytes = 0, sf_stage_bytes = 0;
   size_t smem_bytes = 0;
   size_t ws_partials_bytes = 0, ws_counters_off = 0, ws_counters_bytes = 0, ws_bytes = 0;
+  // K-major copies of M/N-major operands (offsets into the workspace), and
+  // where the split-K part of the workspace starts
+  size_t ws_ta_off = 0, ws_tb_off = 0, ws_split_off = 0;
 };
 
 namespace {
@@ -61,7 +64,11 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int out_size(int out_dtype) { return out_dtype == FP8MM_OUT_F32 ? 4 : 2; }
+int out_size(int out_dtype) {
+  return out_dtype == FP8MM_OUT_F32 ? 4 : (out_dtype == FP8MM_OUT_E4M3 || out_dtype == FP8MM_OUT_E5M2) ? 1 : 2;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Device address of the abort word, looked up once per device (the current
 // device must be `device`).
@@ -173,7 +180,9 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   const fp8mm_desc d = *desc;
   if (d.M < 0 || d.N < 0 || d.K < 0 || d.L < 0) return FP8MM_ERR_INVALID;
   if (d.a_fmt < 0 || d.a_fmt > 1 || d.b_fmt < 0 || d.b_fmt > 1) return FP8MM_ERR_INVALID;
-  if (d.out_dtype < 0 || d.out_dtype > 2) return FP8MM_ERR_INVALID;
+  if (d.out_dtype < 0 || d.out_dtype > 4) return FP8MM_ERR_INVALID;
+  if (d.bias < 0 || d.bias > 1 || d.a_major < 0 || d.a_major > 1 || d.b_major < 0 || d.b_major > 1)
+    return FP8MM_ERR_INVALID;
   if (d.scale_mode < 0 || d.scale_mode > 3) return FP8MM_ERR_INVALID;
   if (d.fast_accum < 0 || d.fast_accum > 1) return FP8MM_ERR_INVALID;
   if (d.splitk < 0 || d.swap_ab < 0 || d.swap_ab > 2 || d.device < 0) return FP8MM_ERR_INVALID;
@@ -186,11 +195,19 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   if (d.M >= lim || d.N >= lim || d.K >= lim || d.L >= 65536) return FP8MM_ERR_UNSUPPORTED;
   if (d.K % 16 != 0) return FP8MM_ERR_ALIGNMENT;
   if ((d.N * out_size(d.out_dtype)) % 16 != 0) return FP8MM_ERR_ALIGNMENT;
+  // M/N-major operands: their rows ([K][M] or [K][N] bytes) must be 16-byte multiples
+  if ((d.a_major && d.M % 16 != 0) || (d.b_major && d.N % 16 != 0)) return FP8MM_ERR_ALIGNMENT;
+  const bool fp8_out = d.out_dtype == FP8MM_OUT_E4M3 || d.out_dtype == FP8MM_OUT_E5M2;
+  // the pages define a bias for bf16 / fp16 (and here fp32) outputs only
+  if (d.bias && fp8_out) return FP8MM_ERR_UNSUPPORTED;
   const bool mx = d.scale_mode == FP8MM_SCALE_MX32_UE8M0;
   if (mx && d.a_fmt != d.b_fmt) return FP8MM_ERR_UNSUPPORTED;
   // torch._scaled_mm refuses E5M2 x E5M2; the library computes it unless the
   // caller asks for torch's refusals.
   if (d.strict_torch && d.a_fmt == FP8MM_E5M2 && d.b_fmt == FP8MM_E5M2) return FP8MM_ERR_REJECTED;
+  // ... and E4M3 x E4M3 -> E5M2 (mmaemu "Testing mmaemu", expected error classes)
+  if (d.strict_torch && d.a_fmt == FP8MM_E4M3 && d.b_fmt == FP8MM_E4M3 && d.out_dtype == FP8MM_OUT_E5M2)
+    return FP8MM_ERR_REJECTED;
 
   fp8mm_plan_s* P = new (std::nothrow) fp8mm_plan_s();
   if (!P) return FP8MM_ERR_INVALID;
@@ -250,22 +267,19 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   const bool auto_pair = d.cta_pair == 0 && !mx && !P->slow && !swap && P->Q > 128 &&
                          (d.block_n == 0 || d.block_n == 224 || d.block_n == 256) &&
                          pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
-  // Slow accumulation on CTA pairs: 256-row tiles of 224 or 256 columns whose
-  // promoted sums stay in registers.  Each SM stages 128 rows of X and half of
-  // Y per 128-K step (32 KiB instead of the 48 KiB of a one-CTA 256-column
-  // tile), and operand staging from L2, not the promotion, is what bounds slow
-  // tiles on GB300.  A 224-column tile's halves (112 columns per epilogue
-  // warp) straddle 128-column scale blocks, so 128x128 Y scales take 256.
+  // Slow accumulation on CTA pairs (256-row held tiles of 224 or 256 columns)
+  // is built but only planned on request (cta_pair = 1): each 128-K chunk is
+  // handed from the pair's MMA to both CTAs' epilogues and back, and on GB300
+  // that round trip made every slow shape measured about 1.7-2x slower than
+  // one-CTA held tiles (4096^3: 146 vs 85 us), although each SM stages a
+  // third fewer operand bytes.  A 224-column tile's halves (112 columns per
+  // epilogue warp) straddle 128-column scale blocks, so 128x128 Y scales
+  // take 256.
   const bool y_block128 = blockwise && P->y_kind == kScaleBlock128;
-  const bool auto_slow_pair = d.cta_pair == 0 && !mx && P->slow && !swap && P->Q > 128 && d.splitk <= 1 &&
-                              (d.epi_warps == 0 || d.epi_warps == 8) &&
-                              (d.block_n == 0 || d.block_n == 256 || (d.block_n == 224 && !y_block128)) &&
-                              pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
-  if (bn == 0 && (auto_pair || auto_slow_pair)) {
+  if (bn == 0 && auto_pair) {
     // the width whose whole waves over the SM pairs cost least
     double best = 1e300;
     for (int c : {256, 224}) {
-      if (auto_slow_pair && c == 224 && y_block128) continue;
       const int64_t tiles = pair_rows * cdiv(P->Q, c) * L;
       const double cost = (double)cdiv(tiles, P->sms / 2) * c / width_efficiency(c, false);
       if (cost < best * 0.999) {
@@ -303,7 +317,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   }
   // Slow accumulation keeps the promoted sums in registers: 256 columns on one
   // CTA or a CTA pair, 224 on a CTA pair only, never swapped, split or MX.
-  const bool pair = d.cta_pair == 1 || auto_pair || auto_slow_pair;
+  const bool pair = d.cta_pair == 1 || auto_pair;
   const bool slow_wide_ok = !swap && !mx && d.splitk <= 1 &&
                             (bn == 256 || (bn == 224 && pair && !y_block128));
   if (P->slow && bn > 128 && !slow_wide_ok) {
@@ -316,9 +330,15 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // factors from a TMEM column aligned to an atom's four columns, so the
   // 224-column kernel gathers Y's factor atoms to start at the tile's first row.
   if (mx && bn != 128 && bn != 224 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
+  // FP8 outputs are stored in rows of at least 16 bytes that start on 16-byte
+  // columns: unswapped tiles of 16 columns (8 per epilogue warp) are too narrow.
+  if (fp8_out && !swap && bn < 32) {
+    if (d.block_n != 0) return FP8MM_ERR_UNSUPPORTED;
+    bn = 32;
+  }
   P->bn = bn;
 
-  if (d.cta_pair == 1 || auto_pair || (auto_slow_pair && bn > 128)) {
+  if (d.cta_pair == 1 || auto_pair) {
     if (mx || swap) return FP8MM_ERR_UNSUPPORTED;
     P->cg = 2;
   }
@@ -439,12 +459,25 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
     }
     P->grid = 2 * (int)std::min<long long>(P->units, nclusters);
   }
+  // Workspace: K-major copies of M/N-major operands first, then the split-K
+  // partial tiles and their arrival counters.
+  size_t ws = 0;
+  if (d.a_major) {
+    P->ws_ta_off = ws;
+    ws += round256((size_t)L * d.M * d.K);
+  }
+  if (d.b_major) {
+    P->ws_tb_off = ws;
+    ws += round256((size_t)L * d.N * d.K);
+  }
+  P->ws_split_off = ws;
   if (P->splits > 1) {
     P->ws_partials_bytes = (size_t)tiles * P->cg * P->splits * kBlockM * bn * sizeof(float);
-    P->ws_counters_off = (P->ws_partials_bytes + 255) & ~(size_t)255;
+    P->ws_counters_off = ws + round256(P->ws_partials_bytes);
     P->ws_counters_bytes = (size_t)tiles * P->cg * sizeof(unsigned);
-    P->ws_bytes = P->ws_counters_off + ((P->ws_counters_bytes + 255) & ~(size_t)255);
+    ws = P->ws_counters_off + round256(P->ws_counters_bytes);
   }
+  P->ws_bytes = ws;
   *out = P;
   P = nullptr;  // ownership passes to the caller
   return FP8MM_OK;
@@ -486,7 +519,8 @@ fp8mm_status fp8mm_plan_roofline(const fp8mm_plan_t* plan, double* flops, double
     default: break;
   }
   *flops = 2.0 * L * M * N * K;
-  *bytes = L * (M * K + N * K) + sbytes + L * M * N * (double)plan->out_es + 4.0;
+  *bytes = L * (M * K + N * K) + sbytes + (d.bias ? N * (double)plan->out_es : 0.0) +
+           L * M * N * (double)plan->out_es + 4.0;
   return FP8MM_OK;
 }
 
@@ -509,7 +543,12 @@ fp8mm_status fp8mm_plan_get_info(const fp8mm_plan_t* plan, fp8mm_plan_info* info
 fp8mm_status fp8mm_plan_kernel_launches(const fp8mm_plan_t* plan, int32_t* launches) {
   if (!plan || !launches) return FP8MM_ERR_INVALID;
   const fp8mm_desc& d = plan->d;
-  *launches = (d.M == 0 || d.N == 0 || d.L == 0 || d.K == 0) ? 0 : 1;
+  if (d.M == 0 || d.N == 0 || d.L == 0)
+    *launches = 0;
+  else if (d.K == 0)
+    *launches = d.bias ? 1 : 0;  // the bias rows (C = 0 is a memset)
+  else
+    *launches = 1 + d.a_major + d.b_major;  // the K-major copies, then the GEMM
   return FP8MM_OK;
 }
 
@@ -536,10 +575,20 @@ fp8mm_status fp8mm_device_error(int device, uint32_t* code, int clear) {
 
 fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void* scale_a, const void* scale_b,
                        void* c, float* amax, void* workspace, size_t workspace_bytes, void* stream_) {
+  return fp8mm_run_ex(P, a, b, scale_a, scale_b, nullptr, nullptr, c, amax, workspace, workspace_bytes, stream_);
+}
+
+fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const void* scale_a, const void* scale_b,
+                          const float* scale_result, const void* bias, void* c, float* amax, void* workspace,
+                          size_t workspace_bytes, void* stream_) {
   if (!P || !amax) return FP8MM_ERR_INVALID;
   const fp8mm_desc& d = P->d;
   const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool empty = d.M == 0 || d.N == 0 || d.L == 0;
+  // a bias exactly when the plan was made for one
+  if ((bias != nullptr) != (d.bias != 0)) return FP8MM_ERR_INVALID;
+  if (bias && !aligned(bias, (uintptr_t)P->out_es)) return FP8MM_ERR_ALIGNMENT;
+  if (scale_result && !aligned(scale_result, 4)) return FP8MM_ERR_ALIGNMENT;
   if (!empty) {
     if (!c) return FP8MM_ERR_INVALID;
     if (d.K > 0 && (!a || !b || !scale_a || !scale_b)) return FP8MM_ERR_INVALID;
@@ -569,9 +618,27 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   if (cudaMemsetAsync(amax, 0, sizeof(float), stream) != cudaSuccess) return FP8MM_ERR_CUDA;
   if (empty) return FP8MM_OK;
   if (d.K == 0) {
-    // An empty sum over K: every element of C is +0.
+    // An empty sum over K: every element of C is +0, plus the bias if any.
+    if (bias)
+      return launch_bias_rows(bias, c, (long long)d.L * d.M, (int)d.N, P->out_es, d.out_dtype == FP8MM_OUT_BF16,
+                              reinterpret_cast<unsigned*>(amax), P->sms, stream) == cudaSuccess
+                 ? FP8MM_OK
+                 : FP8MM_ERR_CUDA;
     const size_t bytes = (size_t)d.L * d.M * d.N * P->out_es;
     return cudaMemsetAsync(c, 0, bytes, stream) == cudaSuccess ? FP8MM_OK : FP8MM_ERR_CUDA;
+  }
+  // M/N-major operands: copy them into K-major workspace, then read the copies.
+  if (d.a_major) {
+    void* ta = static_cast<uint8_t*>(workspace) + P->ws_ta_off;
+    if (launch_transpose_to_kmajor(a, ta, (int)d.L, (int)d.K, (int)d.M, P->sms, stream) != cudaSuccess)
+      return FP8MM_ERR_CUDA;
+    a = ta;
+  }
+  if (d.b_major) {
+    void* tb = static_cast<uint8_t*>(workspace) + P->ws_tb_off;
+    if (launch_transpose_to_kmajor(b, tb, (int)d.L, (int)d.K, (int)d.N, P->sms, stream) != cudaSuccess)
+      return FP8MM_ERR_CUDA;
+    b = tb;
   }
 
   EncodeTiledFn enc = encode_fn();
@@ -625,7 +692,8 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   {
     const CUtensorMapDataType dt = d.out_dtype == FP8MM_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : d.out_dtype == FP8MM_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+                                   : d.out_dtype == FP8MM_OUT_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     cuuint64_t dims[3] = {(cuuint64_t)d.N, (cuuint64_t)d.M, (cuuint64_t)d.L};
     cuuint64_t strides[2] = {(cuuint64_t)(d.N * P->out_es), (cuuint64_t)(d.N * d.M * P->out_es)};
     cuuint32_t es[3] = {1, 1, 1};
@@ -650,6 +718,8 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   kp.swap = P->swap;
   kp.out_dtype = d.out_dtype;
   kp.out_es = P->out_es;
+  kp.scale_result = scale_result;
+  kp.bias = bias;
   kp.stages = P->stages;
   kp.num_acc = P->num_acc;
   kp.tmem_cols = P->tmem_cols;
@@ -684,7 +754,7 @@ fp8mm_status fp8mm_run(fp8mm_plan_t* P, const void* a, const void* b, const void
   kp.abort_word = abort_word_address(d.device);
   if (!kp.abort_word) return FP8MM_ERR_CUDA;
   if (P->splits > 1) {
-    kp.ws_partials = static_cast<float*>(workspace);
+    kp.ws_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + P->ws_split_off);
     kp.ws_counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + P->ws_counters_off);
     if (cudaMemsetAsync(kp.ws_counters, 0, P->ws_counters_bytes, stream) != cudaSuccess) return FP8MM_ERR_CUDA;
   }

@@ -96,10 +96,13 @@ __host__ __device__ constexpr int part_max_cols(int bn, int ew, bool slow = fals
   return ew == 8 ? half0_cols(bn, slow) : bn / 4;
 }
 // Columns of one output chunk (one TMA store of 32 tile rows).
+// FP8 outputs use rows of 32 bytes (16 for held tiles, whose 112-column
+// parts are not multiples of 32).
 __host__ __device__ constexpr int chunk_cols(int bn, int es, int ew, bool held) {
-  return held ? 32 / es
-            : (((ew == 8 ? 64 : 32) / es) < part_max_cols(bn, ew) ? ((ew == 8 ? 64 : 32) / es)
-                                                                   : part_max_cols(bn, ew));
+  return held ? (es == 1 ? 16 : 32 / es)
+         : es == 1 ? (32 < part_max_cols(bn, ew) ? 32 : part_max_cols(bn, ew))
+                   : (((ew == 8 ? 64 : 32) / es) < part_max_cols(bn, ew) ? ((ew == 8 ? 64 : 32) / es)
+                                                                          : part_max_cols(bn, ew));
 }
 // MX: shared-memory bytes per stage for the factor atoms: X's atom and up to
 // three of Y's (a 256-column tile copies whole atoms; a 224-column one has two
@@ -121,8 +124,10 @@ struct KParams {
   int group;              // tile rows per raster group
   long long units;        // L * tiles_r * tiles_q * splits
   int swap;               // 1: C[m][n] is tile(q = m, r = n)
-  int out_dtype;          // 0 f32, 1 bf16, 2 f16
+  int out_dtype;          // 0 f32, 1 bf16, 2 f16, 3 E4M3, 4 E5M2
   int out_es;             // bytes per output element
+  const float* scale_result;  // FP8 outputs: multiplies the result before the FP8 rounding (device), or null
+  const void* bias;       // [N] of out_dtype added to every row before the rounding, or null
   int stages;
   int num_acc;            // TMEM accumulators (1, 2 or 4)
   uint32_t tmem_cols;
@@ -238,22 +243,53 @@ __device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Two fp32 values to two FP8 codes (lo in the low byte): round to nearest
+// even, saturate to the largest finite value (Inf included), NaN stays NaN.
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi, bool e5m2) {
+  uint16_t r;
+  if (e5m2)
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+// Bias value of output column n (bias has out_dtype: fp32, bf16 or fp16).
+__device__ __forceinline__ float bias_at(const KParams& p, int n) {
+  if (p.out_es == 4) return __ldg(static_cast<const float*>(p.bias) + n);
+  const unsigned short h = __ldg(static_cast<const unsigned short*>(p.bias) + n);
+  return p.out_dtype == 1 ? __uint_as_float((uint32_t)h << 16) : __half2float(__ushort_as_half(h));
+}
 
-// Scales CW values of this thread's tile row by alpha, casts them to
-// out_dtype (round to nearest even; NaN becomes the canonical pattern), folds
-// the largest stored |value| into the running amax (inside C only; rounding
-// is monotone, so the largest rounded value is the rounded largest value),
-// stages the warp's 32 x CW block in one of its two shared-memory buffers and
-// stores it with one TMA copy at (cx, cy, cl).
-// v holds at least CW values (the chunk is its first CW); NOSWAP drops the
-// transposed staging of swapped operands from the code.
+// Scales CW values of this thread's tile row by alpha (and adds the bias of
+// each value's output column), casts them to out_dtype (round to nearest
+// even; NaN becomes the canonical pattern; FP8 outputs are multiplied by
+// scale_result first and saturate), folds the largest |value| into the
+// running amax (inside C only; for bf16/fp16/fp32 the largest stored value:
+// rounding is monotone, so it is the rounded largest value; for FP8 outputs
+// the fp32 value before scale_result and the rounding), stages the warp's
+// 32 x CW block in one of its two shared-memory buffers and stores it with one
+// TMA copy at (cx, cy, cl).  xr is the thread's X row (the output column when
+// the operands are swapped).  v holds at least CW values (the chunk is its
+// first CW); NOSWAP drops the transposed staging of swapped operands.
 template <int CW, int ES, int NV, bool NOSWAP = false>
 __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap* tm_c, float (&v)[NV], float alpha,
-                                            bool row_ok, int q0, int lane, uint8_t* stg_gen, uint32_t stg_s,
-                                            int cx, int cy, int cl, bool in_bounds, float& amax_f,
+                                            float sr, bool row_ok, int xr, int q0, int lane, uint8_t* stg_gen,
+                                            uint32_t stg_s, int cx, int cy, int cl, bool in_bounds, float& amax_f,
                                             uint32_t& amax_nan) {
+  if (ES != 1 && p.bias != nullptr) {
+    // d = (a s_a) @ (b s_b)^T + bias: one fp32 fma, then the one rounding to out_dtype
+    if (NOSWAP || !p.swap) {
 #pragma unroll
-  for (int i = 0; i < CW; ++i) v[i] *= alpha;
+      for (int i = 0; i < CW; ++i) v[i] = fmaf(v[i], alpha, (q0 + i < p.Q) ? bias_at(p, q0 + i) : 0.0f);
+    } else {
+      const float bv = row_ok ? bias_at(p, xr) : 0.0f;
+#pragma unroll
+      for (int i = 0; i < CW; ++i) v[i] = fmaf(v[i], alpha, bv);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v[i] *= alpha;
+  }
   // largest |value| of the chunk inside C (NaN-propagating)
   float m = 0.0f;
   if (row_ok && q0 + CW <= p.Q) {
@@ -266,7 +302,29 @@ __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap*
   const bool has_nan = m != m;
   if (lane == 0) ptx::bulk_wait_read_one();  // this buffer's previous store has read it
   __syncwarp();
-  if constexpr (ES == 4) {
+  if constexpr (ES == 1) {
+    // FP8 output: amax of the fp32 values before scale_result (it sets the
+    // next quantisation scale), then one saturating rounding of v * sr.
+    if (!has_nan) amax_f = fmaxf(amax_f, m);
+    const bool e5 = p.out_dtype == 4;
+    uint32_t w[(CW + 3) / 4];
+#pragma unroll
+    for (int i = 0; i < CW / 4; ++i)
+      w[i] = cvt_fp8x2(v[4 * i] * sr, v[4 * i + 1] * sr, e5) | (cvt_fp8x2(v[4 * i + 2] * sr, v[4 * i + 3] * sr, e5) << 16);
+    if (NOSWAP || !p.swap) {
+#pragma unroll
+      for (int c = 0; c < CW / 16; ++c) {
+        const uint32_t off = swz((uint32_t)lane * p.out_rowbytes + c * 16u, p.out_swz_mask);
+        *reinterpret_cast<uint4*>(stg_gen + off) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      }
+    } else if constexpr (!NOSWAP) {
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        const uint32_t off = swz((uint32_t)i * p.out_rowbytes + lane, p.out_swz_mask);
+        stg_gen[off] = (uint8_t)(w[i / 4] >> (8 * (i % 4)));
+      }
+    }
+  } else if constexpr (ES == 4) {
     uint32_t w[CW];
 #pragma unroll
     for (int i = 0; i < CW; ++i) {
@@ -360,6 +418,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   uint32_t amax_nan = 0u;
   bool ok = true;
   const float alpha = p.sa_tensor ? (__ldg(p.sa_tensor) * __ldg(p.sb_tensor)) : 1.0f;
+  const float sr = (ES == 1 && p.scale_result) ? __ldg(p.scale_result) : 1.0f;
   float* ys_w = reinterpret_cast<float*>(sgen + p.off_ys) + warp * HMAX;
   uint8_t* stg = sgen + p.off_out + warp * kStageOut;
   const uint32_t stg_s = sbase + p.off_out + warp * kStageOut;
@@ -644,7 +703,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
           float v[CW];
 #pragma unroll
           for (int i = 0; i < CW; ++i) v[i] = acc(i);
-          store_chunk<CW, ES, CW, true>(p, tm_c, v, alpha, row_ok, q0, lane, stg + stg_sel * (kStageOut / 2),
+          store_chunk<CW, ES, CW, true>(p, tm_c, v, alpha, sr, row_ok, xr, q0, lane, stg + stg_sel * (kStageOut / 2),
                                           stg_s + stg_sel * (kStageOut / 2), q0, r0, t.l, q0 < p.Q && r0 < p.R,
                                           amax_f, amax_nan);
           stg_sel ^= 1u;
@@ -679,7 +738,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
             for (int i = 0; i < CW; ++i) v[i] = sum[i];
           }
           const int q0 = t.tq * BN + col0 + ci * CW;  // Y row of the chunk's first column
-          store_chunk<CW, ES>(p, tm_c, v, alpha, row_ok, q0, lane, stg + stg_sel * (kStageOut / 2),
+          store_chunk<CW, ES>(p, tm_c, v, alpha, sr, row_ok, xr, q0, lane, stg + stg_sel * (kStageOut / 2),
                               stg_s + stg_sel * (kStageOut / 2), p.swap ? r0 : q0, p.swap ? q0 : r0, t.l,
                               q0 < p.Q && r0 < p.R, amax_f, amax_nan);
           stg_sel ^= 1u;
@@ -731,6 +790,12 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
       if (threadIdx.x == 0) atomicOr(p.abort_word, kErrPlan);
       return;
     }
+  }
+  // FP8 outputs store rows of at least 16 bytes starting on 16-byte columns
+  // (a TMA store's rule): unswapped tiles need chunks of 16 columns or more.
+  if (p.out_es == 1 && !p.swap && chunk_cols(BN, 1, EW, held_tile(BN, SLOW, MX)) < 16) {
+    if (threadIdx.x == 0) atomicOr(p.abort_word, kErrPlan);
+    return;
   }
   // CG == 2: a cluster of two CTAs computes 256-row tiles with two-SM MMAs
   // issued by the leader (rank 0); each CTA stages its own 128 rows of X and
@@ -965,6 +1030,10 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
     if constexpr (REGSPLIT) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(epi_regs(EW)));
     if (p.out_es == 4)
       epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 4, EW, held_tile(BN, SLOW, MX)), 4, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+                                                            bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
+                                                            lane);
+    else if (p.out_es == 1)
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 1, EW, held_tile(BN, SLOW, MX)), 1, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
                                                             lane);
     else

@@ -2,9 +2,17 @@
 // table that selects one by tile width, accumulation mode, scale form, CTA
 // pairing and epilogue warp count.
 #pragma once
+#include <cuda_runtime.h>
+
 #include "fp8mm_kernel.cuh"
 
 namespace fp8mm {
+
+// Helper kernels (fp8mm_aux.cu): MN-major operand [L][K][R] -> K-major [L][R][K]
+// scratch; C rows filled with the bias when K = 0.
+cudaError_t launch_transpose_to_kmajor(const void* in, void* out, int L, int K, int R, int sms, cudaStream_t stream);
+cudaError_t launch_bias_rows(const void* bias, void* c, long long rows, int N, int es, int bf16, unsigned* amax_bits,
+                             int sms, cudaStream_t stream);
 
 KernelFn kernel_bn16_fast_f8_cg1_ew8();
 KernelFn kernel_bn32_fast_f8_cg1_ew8();

@@ -82,7 +82,7 @@ int main(void) {
     subprocess.run(["gcc", "-I" + os.path.join(ROOT, "include"), str(src), "-L" + libdir, "-lfp8mm",
                     "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
-    assert out[0].split()[1:] == ["224", "1", "1", "1"]  # held 256 x 224 tiles on a CTA pair
+    assert out[0].split()[1:] == ["256", "0", "1", "1"]
     assert "ALIGN" in out[1].upper()
 
 
@@ -104,7 +104,16 @@ def _plan_status(**kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(M=-1, N=16, K=16), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, a_fmt=2), B.FP8MM_ERR_INVALID),
-    (dict(M=16, N=16, K=16, out_dtype=3), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, out_dtype=5), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, bias=2), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, a_major=2), B.FP8MM_ERR_INVALID),
+    (dict(M=8, N=16, K=16, a_major=1), B.FP8MM_ERR_ALIGNMENT),   # [K][M] rows of 8 bytes
+    (dict(M=16, N=24, K=16, b_major=1), B.FP8MM_ERR_ALIGNMENT),  # [K][N] rows of 24 bytes
+    (dict(M=16, N=8, K=16, out_dtype=3), B.FP8MM_ERR_ALIGNMENT),  # FP8 C rows of 8 bytes
+    (dict(M=16, N=16, K=16, out_dtype=3, bias=1), B.FP8MM_ERR_UNSUPPORTED),  # no bias for FP8 outputs
+    (dict(M=16, N=16, K=16, out_dtype=4, strict_torch=1), B.FP8MM_ERR_REJECTED),  # E4M3 x E4M3 -> E5M2
+    (dict(M=16, N=16, K=16, out_dtype=4), B.FP8MM_OK),
+    (dict(M=16, N=16, K=16, out_dtype=3, a_major=1, b_major=1, bias=0), B.FP8MM_OK),
     (dict(M=16, N=16, K=16, scale_mode=4), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, fast_accum=2), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, block_n=40), B.FP8MM_ERR_INVALID),

@@ -109,8 +109,21 @@ def test_shapes_layout_and_outputs():
         pm.describe(p.a[0], p.b, p.scale_a, p.scale_b, **kw)                         # 2-D with 3-D
     with pytest.raises(ValueError):
         pm.describe(p.a[0], p.b[0, :, :64], p.scale_a, p.scale_b, **kw)              # K differs
+    # a b stored [K, N] (N innermost) is an N-major operand: accepted, copied K-major by the library
+    assert pm.describe(p.a[0], p.b[0].t().contiguous().t(), p.scale_a, p.scale_b, **kw)[:4] == (1, 32, 48, 128)
+    assert pm.operand_majors(p.a[0].t().contiguous().t(), p.b[0].t().contiguous().t()) == (1, 1)
+    with pytest.raises(ValueError):                                                  # N-major with N % 16
+        q = synth.llm_per_tensor(M=32, N=40, K=128)
+        pm.describe(q.a[0], q.b[0].t().contiguous().t(), q.scale_a, q.scale_b, **kw)
+    with pytest.raises(ValueError):                                                  # neither axis contiguous
+        pm.describe(p.a[0], torch.empty(48, 256, dtype=torch.uint8)[:, ::2], p.scale_a, p.scale_b, **kw)
+    with pytest.raises(ValueError):                                                  # bias of the wrong dtype
+        pm.describe(p.a[0], p.b[0], p.scale_a, p.scale_b, bias=torch.zeros(48), **kw)
+    with pytest.raises(ValueError):                                                  # no bias with FP8 outputs
+        pm.describe(p.a[0], p.b[0], p.scale_a, p.scale_b, out_dtype=torch.float8_e4m3fn,
+                    bias=torch.zeros(48, dtype=torch.float8_e4m3fn), **kw)
     with pytest.raises(ValueError):
-        pm.describe(p.a[0], p.b[0].t().contiguous().t(), p.scale_a, p.scale_b, **kw)  # not K-contiguous
+        pm.describe(p.a[0], p.b[0], p.scale_a, p.scale_b, scale_result=torch.ones(2), **kw)
     with pytest.raises(ValueError):
         pm.describe(p.a[0], p.b[0], p.scale_a, p.scale_b.to("meta"), **kw)           # another device
     with pytest.raises(ValueError):
@@ -130,7 +143,7 @@ def test_scaled_mm_refuses_host_tensors():
 
 
 def test_plan_keys_of_every_length_agree():
-    full = (64, 64, 128, 1, 0, 0, 0, 1, 1, 0, 0, 0, 0, 0, 0, 0)
+    full = (64, 64, 128, 1, 0, 0, 0, 1, 1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
     assert pm.normalize_key(full[:13]) == full      # without pair, epilogue warps or strictness
     assert pm.normalize_key(full[:14]) == full
     assert pm.normalize_key(full[:15]) == full

@@ -2,8 +2,11 @@
 
 ``torch_scaled_mm`` only rearranges arguments for ``scaled_mm``: mat2 [K, N]
 column-major becomes the [N, K] K-contiguous operand (same storage), the
-scales are tensor-wise, and torch's refusal of E5M2 x E5M2 is requested from
-the planner.  The device call is replaced here by a recorder.
+scales are tensor-wise, bias and scale_result (read for FP8 outputs only) are
+passed on, and torch's refusals (E5M2 x E5M2, E4M3 x E4M3 -> E5M2) are
+requested from the planner.  ``bmm_fp8`` passes b as a [B, N, K] view
+whatever its axis order; the library copies an N-innermost b into K-major
+workspace.  The device call is replaced here by a recorder.
 """
 import pytest
 import torch
@@ -37,26 +40,27 @@ def test_column_major_mat2_becomes_the_k_contiguous_operand(calls):
     assert pm.torch_scaled_mm(a, w.t(), sa, sb, out_dtype=torch.bfloat16, use_fast_accum=True, out=out) == "C"
     (a2, b2, sa2, sb2, kw), = calls
     assert a2 is a and b2.shape == (48, 64) and b2.is_contiguous() and b2.data_ptr() == w.data_ptr()
-    assert sa2 is sa and sb2 is sb
+    assert sa2.shape == (1,) and sb2.shape == (1,) and sa2.data_ptr() == sa.data_ptr()
     assert kw == dict(out_dtype=torch.bfloat16, use_fast_accum=True, scale_mode=pm.FP8MM_SCALE_TENSOR, out=out,
-                      strict_torch=True)
+                      strict_torch=True, bias=None, scale_result=None)
 
 
 def test_defaults_follow_torch(calls):
     a, w, sa, sb = _operands()
-    with pytest.raises(NotImplementedError):           # out_dtype defaults to input's FP8 dtype
-        pm.torch_scaled_mm(a, w.t(), sa, sb)
+    pm.torch_scaled_mm(a, w.t(), sa, sb)               # out_dtype defaults to input's FP8 dtype
+    assert calls[-1][4]["out_dtype"] == torch.float8_e4m3fn and calls[-1][4]["scale_result"] is None
     pm.torch_scaled_mm(a, w.t(), sa, sb, None, torch.tensor([2.0]), torch.float32)  # positional; scale_result ignored
     kw = calls[-1][4]
-    assert kw["use_fast_accum"] is False and kw["out_dtype"] == torch.float32
+    assert kw["use_fast_accum"] is False and kw["out_dtype"] == torch.float32 and kw["scale_result"] is None
+    pm.torch_scaled_mm(a, w.t(), sa, sb, None, torch.tensor(2.0), torch.float8_e4m3fn)   # read for FP8 outputs
+    assert float(calls[-1][4]["scale_result"]) == 2.0 and calls[-1][4]["scale_result"].shape == (1,)
+    bias = torch.zeros(48, dtype=torch.bfloat16)
+    pm.torch_scaled_mm(a, w.t(), sa, sb, bias=bias, out_dtype=torch.bfloat16)
+    assert calls[-1][4]["bias"] is bias
 
 
 def test_refusals(calls):
     a, w, sa, sb = _operands()
-    with pytest.raises(NotImplementedError):
-        pm.torch_scaled_mm(a, w.t(), sa, sb, bias=torch.zeros(48), out_dtype=torch.bfloat16)
-    with pytest.raises(NotImplementedError):
-        pm.torch_scaled_mm(a, w.t(), sa, sb, out_dtype=torch.float8_e5m2)
     with pytest.raises(NotImplementedError):
         pm.torch_scaled_mm(a, w.t(), torch.ones(32, 1), torch.ones(1, 48), out_dtype=torch.bfloat16)
     with pytest.raises(ValueError):                    # row-major [K, N]
@@ -88,15 +92,24 @@ def test_bmm_b_in_either_axis_order_is_read_in_place(calls):
         assert kw["use_fast_accum"] is False
 
 
-def test_bmm_refuses_k_outermost_b_and_bad_shapes(calls):
+def test_bmm_passes_an_n_innermost_b_as_a_transposed_view(calls):
     g = torch.Generator().manual_seed(9)
     a = torch.randn(3, 16, 64, generator=g).to(torch.float8_e4m3fn)
-    bkn = torch.randn(3, 64, 24, generator=g).to(torch.float8_e4m3fn)   # [B, K, N] with N innermost
+    bkn = torch.randn(3, 64, 32, generator=g).to(torch.float8_e4m3fn)   # [B, K, N] with N innermost
+    s = torch.tensor(1.0)
+    pm.bmm_fp8(a, bkn, s, s)
+    (a2, b2, _, _, _), = calls
+    assert b2.shape == (3, 32, 64) and not b2.is_contiguous() and b2.transpose(1, 2).is_contiguous()
+    assert pm.operand_majors(a2, b2) == (0, 1)                          # the library copies it K-major
+
+
+def test_bmm_refuses_bad_shapes(calls):
+    g = torch.Generator().manual_seed(9)
+    a = torch.randn(3, 16, 64, generator=g).to(torch.float8_e4m3fn)
+    bkn = torch.randn(3, 64, 24, generator=g).to(torch.float8_e4m3fn)
     s = torch.tensor(1.0)
     with pytest.raises(ValueError):
-        pm.bmm_fp8(a, bkn, s, s)
-    with pytest.raises(ValueError):
-        pm.bmm_fp8(a, bkn.transpose(1, 2).contiguous(), s, s)           # [B, N, K] without trans_b
+        pm.bmm_fp8(a, bkn.transpose(1, 2).contiguous(), s, s)           # [B, N, K] without trans_b: K mismatch
     with pytest.raises(ValueError):
         pm.bmm_fp8(a[:2], bkn.transpose(1, 2).contiguous(), s, s, trans_b=True)
     with pytest.raises(ValueError):
