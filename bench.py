@@ -13,7 +13,10 @@ metric is quoted on, each with its own synthetic inputs resident in HBM:
 every call with the fused amax.  ``value`` is the whole step's TFLOP/s (all
 calls' flops over the sum of their device times); ``per_config`` reports every
 call against its own roofline (tensor-bound: of the FP8 peak; HBM-bound: of
-the copy bandwidth); ``roofline`` is the dominant call of the step.  ``e2e``
+the copy bandwidth); ``roofline`` is the dominant call of the step.
+``next_rows`` times, apart from the step, the forms beyond the five
+configurations: an FP8 output, a bias, the NN layout, NVFP4 / MXFP4 operands
+and a batched GEMM with b given K-outermost.  ``e2e``
 is the same metric through the public API with each call's operands copied
 from pinned host memory and C and amax read back, inside the timed region.
 ``--impl reference`` times the CPU oracle instead (a bounded sample of every
@@ -41,6 +44,7 @@ METRIC = "FP8 scaled-GEMM TFLOP/s (+GB/s) at 1 GB300 and % of FP8/HBM roofline"
 KERNEL_SOURCES = ["precision_matmul_gb300/csrc/fp8mm_kernel.cuh", "precision_matmul_gb300/csrc/ptx.cuh"]
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 FP8_NOMINAL_TFLOPS = 4500.0
+FP4_PER_BF16 = 6.0  # nominal dense FP4 : BF16 tensor rate on GB300 (13.5 : 2.25 PFLOP/s)
 L2_BYTES = 129 * 10 ** 6
 SKINNY_M = (16, 64, 256, 1024, 2048, 8192)
 
@@ -68,6 +72,19 @@ def _catalogue():
                        lambda: synth.mx_batched(fmt=synth.E4M3)),
         "c4_mx_e5m2": ("MX 4 x 4096^3 E5M2, UE8M0 per 32 along K, fp32 out",
                        lambda: synth.mx_batched(fmt=synth.E5M2)),
+        # rows beyond the five configurations (timed apart from the metric's step)
+        "n1_fp8out_e4m3_4096": ("per-tensor E4M3 4096^3, E4M3 out with scale_result, fast",
+                                lambda: _fp8out_4096()),
+        "n2_bias_bf16_4096": ("per-tensor E4M3 4096^3, bf16 out + bias [N], fast",
+                              lambda: synth.llm_per_tensor(fast_accum=True)),
+        "n2_layout_nn_4096": ("per-tensor E4M3 4096^3 NN (b stored [K][N]: K-major copy first), bf16, fast",
+                              lambda: synth.llm_per_tensor(fast_accum=True)),
+        "n3_nvfp4_4x4096": ("NVFP4 4 x 4096^3 (E2M1, E4M3 factors per 16), fp32 out",
+                            lambda: synth.fp4_batched(form="nv16")),
+        "n3_mxfp4_4x4096": ("MXFP4 4 x 4096^3 (E2M1, UE8M0 factors per 32), fp32 out",
+                            lambda: synth.fp4_batched(form="mx32")),
+        "n4_bmm_bkn_4x4096": ("batched per-tensor E4M3 4 x 4096^3 with b as [B][K][N] (BmmFP8FwdOp), bf16",
+                              lambda: synth.llm_per_tensor(L=4, fast_accum=True)),
     }
     for M in SKINNY_M:
         for fast in (True, False):
@@ -77,6 +94,21 @@ def _catalogue():
             cat[f"c5_skinny_M{M}_adv_{mode}"] = (
                 f"per-tensor E4M3 M={M} N=28672 K=8192 adversarial, bf16 out, {mode}", (M, "adversarial", fast))
     return cat
+
+
+# extra arguments of the next-row calls
+EXTRA = {"n1_fp8out_e4m3_4096": {"scale_result": 1.0}, "n2_bias_bf16_4096": {"bias": True},
+         "n2_layout_nn_4096": {"b_major": True}, "n4_bmm_bkn_4x4096": {"b_major": True}}
+NEXT = ["n1_fp8out_e4m3_4096", "n2_bias_bf16_4096", "n2_layout_nn_4096", "n3_nvfp4_4x4096", "n3_mxfp4_4x4096",
+        "n4_bmm_bkn_4x4096"]
+
+
+def _fp8out_4096():
+    from precision_matmul_gb300 import synth
+    p = synth.llm_per_tensor(fast_accum=True, out_dtype=synth.OUT_E4M3)
+    p.scale_a.fill_(2.0 ** -8)
+    p.scale_b.fill_(2.0 ** -7)
+    return p
 
 
 DEFAULT = (["c1_tiny_256", "c2_llm4096_fast", "c2_llm4096_slow", "c3_blockwise", "c4_mx_e4m3", "c4_mx_e5m2"] +
@@ -90,6 +122,7 @@ GROUPS = {
     "c4": ["c4_mx_e4m3", "c4_mx_e5m2"], "mx": ["c4_mx_e4m3", "c4_mx_e5m2"],
     "mx_e4m3": ["c4_mx_e4m3"], "mx_e5m2": ["c4_mx_e5m2"],
     "c5": [f"c5_skinny_M{M}_{m}" for M in SKINNY_M for m in ("fast", "slow")],
+    "next": NEXT,
 }
 for _M in SKINNY_M:
     GROUPS[f"skinny_{_M}"] = [f"c5_skinny_M{_M}_fast", f"c5_skinny_M{_M}_slow"]
@@ -349,20 +382,35 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device(f"cuda:{local_rank}")
     probs = problems(args.workload)
-    ins = []
-    dev_inputs = {}
-    for name, _, p in probs:
-        key = id(p.a)
-        if key not in dev_inputs:  # fast/slow calls of one draw share their device operands
-            dev_inputs[key] = (p.a.to(dev), p.b.to(dev), p.scale_a.to(dev), p.scale_b.to(dev))
-        a, b, sa, sb = dev_inputs[key]
-        squeeze = p.L == 1
-        if squeeze:
-            a, b = a[0], b[0]
-        shape = (p.M, p.N) if squeeze else (p.L, p.M, p.N)
-        c = torch.empty(shape, dtype=synth.OUT_TORCH[p.out_dtype], device=dev)
-        amax = torch.empty(1, dtype=torch.float32, device=dev)
-        ins.append((p, a, b, sa, sb, c, amax))
+    next_probs = problems("next") if (args.next_rows and args.workload == "all") else []
+
+    def prepare(plist):
+        items = []
+        dev_inputs = {}
+        for name, _, p in plist:
+            key = id(p.a)
+            if key not in dev_inputs:  # fast/slow calls of one draw share their device operands
+                dev_inputs[key] = (p.a.to(dev), p.b.to(dev), p.scale_a.to(dev), p.scale_b.to(dev))
+            a, b, sa, sb = dev_inputs[key]
+            squeeze = p.L == 1
+            if squeeze:
+                a, b = a[0], b[0]
+            ex = EXTRA.get(name, {})
+            kw = {}
+            if ex.get("b_major"):  # b stored [.., K, N]: the library copies it K-major first
+                b = b.transpose(-1, -2).contiguous().transpose(-1, -2)
+            if ex.get("bias"):
+                g = torch.Generator().manual_seed(11)
+                kw["bias"] = (torch.randn(p.N, generator=g) * 100).to(synth.OUT_TORCH[p.out_dtype]).to(dev)
+            if "scale_result" in ex:
+                kw["scale_result"] = torch.tensor([ex["scale_result"]], dtype=torch.float32, device=dev)
+            shape = (p.M, p.N) if squeeze else (p.L, p.M, p.N)
+            c = torch.empty(shape, dtype=synth.OUT_TORCH[p.out_dtype], device=dev)
+            amax = torch.empty(1, dtype=torch.float32, device=dev)
+            items.append((p, a, b, sa, sb, c, amax, kw))
+        return items
+
+    ins = prepare(probs)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
     sink = torch.empty(1, dtype=torch.int64, device=dev)
 
@@ -375,9 +423,9 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
 
     def call(item):
-        p, a, b, sa, sb, c, amax = item
+        p, a, b, sa, sb, c, amax, kw = item
         pm.scaled_mm(a, b, sa, sb, out_dtype=synth.OUT_TORCH[p.out_dtype], use_fast_accum=p.fast_accum,
-                     a_fmt=p.a_fmt, b_fmt=p.b_fmt, scale_mode=p.scale_mode, out=c, amax=amax)
+                     a_fmt=p.a_fmt, b_fmt=p.b_fmt, scale_mode=p.scale_mode, out=c, amax=amax, **kw)
 
     for _ in range(args.warmup):
         for it in ins:
@@ -412,6 +460,30 @@ def run_ours(args, rank, world, local_rank):
     if err:
         raise SystemExit(f"device abort recorded: {err:#x}")
 
+    # ---- the next rows (not part of the metric's step): same timing, own loop
+    next_call = []
+    if next_probs:
+        nxt = prepare(next_probs)
+        next_call = [[] for _ in nxt]
+        for _ in range(3):
+            for it in nxt:
+                call(it)
+        nev = []
+        for _ in range(args.next_steps):
+            for i, it in enumerate(nxt):
+                flush_l2()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call(it)
+                e1.record(stream)
+                nev.append((i, e0, e1))
+        torch.cuda.synchronize()
+        for i, e0, e1 in nev:
+            next_call[i].append(e0.elapsed_time(e1) / 1e3)
+        del nxt
+        if pm.fp8mm_device_error(local_rank):
+            raise SystemExit("device abort recorded in the next-row calls")
+
     # ---- sustained: the dominant call back to back for >= sustain_s under the clock sampler
     call_s = [sum(x) / len(x) for x in per_call]
     dom = max(range(len(probs)), key=lambda i: call_s[i])
@@ -436,19 +508,19 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- e2e through the public API: pinned host operands in, C and amax out
     host = []
-    for p, a, b, sa, sb, c, amax in ins:
+    for p, a, b, sa, sb, c, amax, _ in ins:
         host.append((a.cpu().pin_memory(), b.cpu().pin_memory(), sa.cpu().pin_memory(), sb.cpu().pin_memory(),
                      torch.empty(c.shape, dtype=c.dtype).pin_memory(), torch.empty(1, dtype=torch.float32).pin_memory()))
     h2d = sum(sum(t.numel() * t.element_size() for t in x[:4]) for x in host)
     d2h = sum(x[4].numel() * x[4].element_size() + 4 for x in host)
 
     def e2e_step():
-        for (ha, hb, hsa, hsb, hc, hm), (p, a, b, sa, sb, c, amax) in zip(host, ins):
+        for (ha, hb, hsa, hsb, hc, hm), (p, a, b, sa, sb, c, amax, kw) in zip(host, ins):
             a.copy_(ha, non_blocking=True)
             b.copy_(hb, non_blocking=True)
             sa.copy_(hsa, non_blocking=True)
             sb.copy_(hsb, non_blocking=True)
-            call((p, a, b, sa, sb, c, amax))
+            call((p, a, b, sa, sb, c, amax, kw))
             hc.copy_(c, non_blocking=True)
             hm.copy_(amax, non_blocking=True)
 
@@ -471,24 +543,37 @@ def run_ours(args, rank, world, local_rank):
     fp8_peak = bf16 * FP8_PER_BF16
     cublas = cublas_fp8_peak(dev) if args.cublas_peak else None
     traffic = read_traffic()
-    plans = [pm.plan_for((p.M, p.N, p.K, p.L, p.a_fmt, p.b_fmt, p.scale_mode, p.out_dtype,
-                          1 if p.fast_accum else 0, 0, 0, 0, local_rank, 0)) for _, _, p in probs]
+    def plan_of(name, p):
+        ex = EXTRA.get(name, {})
+        return pm.plan_for((p.M, p.N, p.K, p.L, p.a_fmt, p.b_fmt, p.scale_mode, p.out_dtype,
+                            1 if p.fast_accum else 0, 0, 0, 0, local_rank, 0, 0, 0, 1 if ex.get("bias") else 0, 0,
+                            1 if ex.get("b_major") else 0))
+
+    def entries(plist, times):
+        out = []
+        for (name, desc, p), ts in zip(plist, times):
+            pl = plan_of(name, p)
+            f, by = pl.roofline()
+            med = statistics.median(ts)
+            # FP4 operands run on the FP4 tensor rate (nominal 13.5 : 2.25 against bf16)
+            peak = bf16 * (FP4_PER_BF16 if p.a_fmt == synth.E2M1 else FP8_PER_BF16)
+            tensor_bound = f / (peak * 1e12) >= by / (hbm * 1e9)
+            tf, gbs = f / med / 1e12, by / med / 1e9
+            entry = {"name": name, "what": desc, "us": med * 1e6, "tflops": tf, "gbs": gbs,
+                     "bound": "tensor" if tensor_bound else "hbm", "peak": peak if tensor_bound else hbm,
+                     "frac": tf / peak if tensor_bound else gbs / hbm,
+                     "roofline_us": max(f / (peak * 1e12), by / (hbm * 1e9)) * 1e6,
+                     "plan": pl.info(), "kernel_launches": pl.kernel_launches(), "traffic": traffic.get(name)}
+            if isinstance(cublas, float) and tensor_bound and p.a_fmt != synth.E2M1:
+                entry["frac_of_cublas_fp8"] = tf / cublas
+                entry["frac_of_nominal_fp8"] = tf / FP8_NOMINAL_TFLOPS
+            out.append(entry)
+        return out
+
+    plans = [plan_of(n, p) for n, _, p in probs]
     launches = sum(pl.kernel_launches() for pl in plans)
-    per_config = []
-    for i, ((name, desc, p), pl) in enumerate(zip(probs, plans)):
-        f, by = pl.roofline()
-        med = statistics.median(per_call[i])
-        tensor_bound = f / (fp8_peak * 1e12) >= by / (hbm * 1e9)
-        tf, gbs = f / med / 1e12, by / med / 1e9
-        entry = {"name": name, "what": desc, "us": med * 1e6, "tflops": tf, "gbs": gbs,
-                 "bound": "tensor" if tensor_bound else "hbm",
-                 "frac": tf / fp8_peak if tensor_bound else gbs / hbm,
-                 "roofline_us": max(f / (fp8_peak * 1e12), by / (hbm * 1e9)) * 1e6,
-                 "plan": pl.info(), "traffic": traffic.get(name)}
-        if isinstance(cublas, float) and tensor_bound:
-            entry["frac_of_cublas_fp8"] = tf / cublas
-            entry["frac_of_nominal_fp8"] = tf / FP8_NOMINAL_TFLOPS
-        per_config.append(entry)
+    per_config = entries(probs, per_call)
+    next_rows = entries(next_probs, next_call) if next_probs else None
     d = per_config[dom]
     roof = {"bound": d["bound"], "achieved": d["tflops"] if d["bound"] == "tensor" else d["gbs"],
             "peak": fp8_peak if d["bound"] == "tensor" else hbm,
@@ -513,6 +598,7 @@ def run_ours(args, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "/".join(fmts) + " operands, fp32 accumulation", "data": "synthetic",
             "config": cfg, "per_config": per_config, "roofline": roof,
+            "next_rows": next_rows,
             "peaks": {"fp8_tflops_used": fp8_peak, "hbm_gbs_used": hbm, "source": peak_src,
                       "fp8_nominal_dense_tflops": FP8_NOMINAL_TFLOPS, "cublas_fp8_8192cubed_tflops": cublas,
                       "fp8_sustained_from_bf16_tflops": bf16_sus * FP8_PER_BF16},
@@ -534,6 +620,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--sustain-s", type=float, default=2.0)
     ap.add_argument("--no-cublas-peak", dest="cublas_peak", action="store_false")
+    ap.add_argument("--no-next-rows", dest="next_rows", action="store_false")
+    ap.add_argument("--next-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

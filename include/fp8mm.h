@@ -46,6 +46,11 @@
  *                                  512-byte atom, byte i32*16 + i4*4 + j4 scales row
  *                                  i32 + 32*i4 of the 128-row block and the 32-element
  *                                  K block j4 of the 128-element K block.
+ *     FP8MM_SCALE_NV16_E4M3        (FP4 operands only) E4M3 factor codes, positive (the
+ *                                  tensor core reads them as unsigned E4M3), one per 16
+ *                                  elements of K, in the same atoms: [L][ceil(rows/128)]
+ *                                  [ceil(K/64)][32][4][4], j4 the 16-element block of the
+ *                                  64-element K block.
  *
  * Ownership: the caller owns every buffer (inputs, outputs, workspace) and
  * every pointer above is a DEVICE pointer on the plan's device.  A plan holds
@@ -71,7 +76,12 @@
 extern "C" {
 #endif
 
-typedef enum { FP8MM_E4M3 = 0, FP8MM_E5M2 = 1 } fp8mm_fmt;
+/* Operand formats.  FP8MM_E2M1 is packed FP4 (float4_e2m1fn_x2: two values per
+ * byte along K, element 2i in the low four bits of byte i; cuDNN "GEMM + Amax
+ * (SM100)", Dtypes and Layouts): A and B both E2M1, K-major, K % 64 == 0, a
+ * block-scaled form (FP8MM_SCALE_MX32_UE8M0 = MXFP4 or FP8MM_SCALE_NV16_E4M3
+ * = NVFP4), fast accumulation; a and b then hold K/2 bytes per row. */
+typedef enum { FP8MM_E4M3 = 0, FP8MM_E5M2 = 1, FP8MM_E2M1 = 2 } fp8mm_fmt;
 
 /* FP8 outputs (E4M3, E5M2): C = round_sat(fp32(alpha * acc) * scale_result), rounded once to
  * nearest even and saturated to the largest finite value (NaN stays NaN); amax is then
@@ -89,7 +99,8 @@ typedef enum {
   FP8MM_SCALE_TENSOR = 0,
   FP8MM_SCALE_A1x128_B1x128 = 1,
   FP8MM_SCALE_A1x128_B128x128 = 2,
-  FP8MM_SCALE_MX32_UE8M0 = 3
+  FP8MM_SCALE_MX32_UE8M0 = 3,
+  FP8MM_SCALE_NV16_E4M3 = 4
 } fp8mm_scale_mode;
 
 typedef enum {

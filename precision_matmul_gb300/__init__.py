@@ -20,14 +20,15 @@ from __future__ import annotations
 import threading
 
 from . import _binding
-from ._binding import (FP8MM_E4M3, FP8MM_E5M2, FP8MM_OUT_BF16, FP8MM_OUT_E4M3, FP8MM_OUT_E5M2, FP8MM_OUT_F16,
+from ._binding import (FP8MM_E2M1, FP8MM_E4M3, FP8MM_E5M2, FP8MM_OUT_BF16, FP8MM_OUT_E4M3, FP8MM_OUT_E5M2, FP8MM_OUT_F16,
                        FP8MM_OUT_F32, FP8MM_SCALE_A1x128_B1x128, FP8MM_SCALE_A1x128_B128x128,
-                       FP8MM_SCALE_MX32_UE8M0, FP8MM_SCALE_TENSOR, FP8MMError, Plan, fp8mm_device_error,
+                       FP8MM_SCALE_MX32_UE8M0, FP8MM_SCALE_NV16_E4M3, FP8MM_SCALE_TENSOR, FP8MMError, Plan, fp8mm_device_error,
                        fp8mm_gemm, fp8mm_plan, fp8mm_run, fp8mm_run_ex, fp8mm_status_string, make_desc)
 
 __all__ = ["scaled_mm", "torch_scaled_mm", "bmm_fp8", "describe", "operand_majors", "plan_for", "Plan", "FP8MMError",
            "fp8mm_plan", "fp8mm_run", "fp8mm_run_ex", "fp8mm_gemm",
-           "fp8mm_device_error", "fp8mm_status_string", "make_desc", "FP8MM_E4M3", "FP8MM_E5M2",
+           "fp8mm_device_error", "fp8mm_status_string", "make_desc", "FP8MM_E4M3", "FP8MM_E5M2", "FP8MM_E2M1",
+           "FP8MM_SCALE_NV16_E4M3",
            "FP8MM_OUT_F32", "FP8MM_OUT_BF16", "FP8MM_OUT_F16", "FP8MM_OUT_E4M3", "FP8MM_OUT_E5M2", "FP8MM_SCALE_TENSOR",
            "FP8MM_SCALE_A1x128_B1x128", "FP8MM_SCALE_A1x128_B128x128", "FP8MM_SCALE_MX32_UE8M0"]
 
@@ -43,15 +44,19 @@ def _torch():
 
 def _fmt_of(t, explicit):
     torch = _torch()
-    native = {torch.float8_e4m3fn: FP8MM_E4M3, torch.float8_e5m2: FP8MM_E5M2}.get(t.dtype)
+    table = {torch.float8_e4m3fn: FP8MM_E4M3, torch.float8_e5m2: FP8MM_E5M2}
+    if hasattr(torch, "float4_e2m1fn_x2"):
+        table[torch.float4_e2m1fn_x2] = FP8MM_E2M1
+    native = table.get(t.dtype)
     if native is None and t.dtype != torch.uint8:
-        raise TypeError(f"operand dtype {t.dtype}: pass float8_e4m3fn / float8_e5m2, or uint8 codes with a_fmt/b_fmt")
+        raise TypeError(f"operand dtype {t.dtype}: pass float8_e4m3fn / float8_e5m2 / float4_e2m1fn_x2, or uint8 "
+                        "codes with a_fmt/b_fmt")
     if explicit is None:
         if native is None:
             raise TypeError("uint8 operand codes need their format (a_fmt / b_fmt)")
         return native
-    if int(explicit) not in (FP8MM_E4M3, FP8MM_E5M2):
-        raise ValueError(f"format {explicit}: FP8MM_E4M3 or FP8MM_E5M2")
+    if int(explicit) not in (FP8MM_E4M3, FP8MM_E5M2, FP8MM_E2M1):
+        raise ValueError(f"format {explicit}: FP8MM_E4M3, FP8MM_E5M2 or FP8MM_E2M1")
     if native is not None and int(explicit) != native:
         raise ValueError(f"operand dtype {t.dtype} contradicts format {explicit}")
     return int(explicit)
@@ -91,8 +96,9 @@ def _mx_dtypes():
 def _scale_elems(mode, L, M, N, K):
     """Elements of (scale_a, scale_b) that the kernels read for a scale form:
     one fp32 each per tensor; fp32 [L][M][ceil(K/128)] for 1x128 A scales and
-    [L][N][..] / [L][ceil(N/128)][..] for B; one 512-byte UE8M0 atom per 128
-    rows and 128 K for MX factors."""
+    [L][N][..] / [L][ceil(N/128)][..] for B; one 512-byte atom per 128 rows
+    and 4 factors along K for the factor forms (128 K for UE8M0 per 32, 64 K
+    for E4M3 per 16)."""
     kb = (K + 127) // 128
     if mode == FP8MM_SCALE_TENSOR:
         return 1, 1
@@ -102,10 +108,16 @@ def _scale_elems(mode, L, M, N, K):
         return L * M * kb, L * ((N + 127) // 128) * kb
     if mode == FP8MM_SCALE_MX32_UE8M0:
         return L * ((M + 127) // 128) * kb * 512, L * ((N + 127) // 128) * kb * 512
+    if mode == FP8MM_SCALE_NV16_E4M3:
+        k64 = (K + 63) // 64
+        return L * ((M + 127) // 128) * k64 * 512, L * ((N + 127) // 128) * k64 * 512
     raise ValueError(f"scale_mode {mode}: one of the FP8MM_SCALE_* forms")
 
 
 def _infer_scale_mode(scale_a, scale_b, L, M, N, K):
+    torch = _torch()
+    if scale_a.dtype == torch.float8_e4m3fn:
+        return FP8MM_SCALE_NV16_E4M3
     if scale_a.dtype in _mx_dtypes():
         return FP8MM_SCALE_MX32_UE8M0
     if scale_a.numel() == 1 and scale_b.numel() == 1:
@@ -136,10 +148,15 @@ def describe(a, b, scale_a, scale_b, *, out_dtype=None, a_fmt=None, b_fmt=None, 
     if a.dim() not in (2, 3) or b.dim() != a.dim():
         raise ValueError("a and b must both be [M, K] or both [L, M, K]")
     L = a.shape[0] if batched else 1
+    fa, fb = _fmt_of(a, a_fmt), _fmt_of(b, b_fmt)
     M, K = a.shape[-2], a.shape[-1]
     N = b.shape[-2]
     if b.shape[-1] != K or (batched and b.shape[0] != L):
         raise ValueError("a and b disagree on K or L")
+    if fa == FP8MM_E2M1 or fb == FP8MM_E2M1:
+        if fa != fb:
+            raise ValueError("FP4 operands go in pairs (A and B of one format)")
+        K *= 2  # packed: two elements per byte
     others = [scale_a, scale_b] + [t for t in (out, amax, bias, scale_result) if t is not None]
     if any(t.device != a.device for t in [a, b] + others):
         raise ValueError("all tensors must be on one device")
@@ -148,7 +165,6 @@ def describe(a, b, scale_a, scale_b, *, out_dtype=None, a_fmt=None, b_fmt=None, 
     am, bm = operand_majors(a, b)
     if (am and M % 16) or (bm and N % 16):
         raise ValueError("a K-outermost operand needs rows (M or N) that are multiples of 16")
-    fa, fb = _fmt_of(a, a_fmt), _fmt_of(b, b_fmt)
     oc = _out_code(out_dtype)
     mode = int(scale_mode) if scale_mode is not None else _infer_scale_mode(scale_a, scale_b, L, M, N, K)
     want_a, want_b = _scale_elems(mode, L, M, N, K)
@@ -157,6 +173,11 @@ def describe(a, b, scale_a, scale_b, *, out_dtype=None, a_fmt=None, b_fmt=None, 
             raise TypeError("MX factors are uint8 / float8_e8m0fnu UE8M0 codes")
         if fa != fb:
             raise ValueError("the MX form needs A and B of one format")
+    elif mode == FP8MM_SCALE_NV16_E4M3:
+        if scale_a.dtype not in (torch.uint8, torch.float8_e4m3fn) or scale_b.dtype != scale_a.dtype:
+            raise TypeError("per-16 factors are uint8 / float8_e4m3fn E4M3 codes")
+        if fa != FP8MM_E2M1:
+            raise ValueError("factors per 16 elements go with FP4 operands")
     elif scale_a.dtype != torch.float32 or scale_b.dtype != torch.float32:
         raise TypeError("per-tensor and block scales are float32")
     if (scale_a.numel(), scale_b.numel()) != (want_a, want_b):

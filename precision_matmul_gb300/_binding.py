@@ -12,10 +12,10 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfp8mm.so")
 
-FP8MM_E4M3, FP8MM_E5M2 = 0, 1
+FP8MM_E4M3, FP8MM_E5M2, FP8MM_E2M1 = 0, 1, 2
 FP8MM_OUT_F32, FP8MM_OUT_BF16, FP8MM_OUT_F16, FP8MM_OUT_E4M3, FP8MM_OUT_E5M2 = 0, 1, 2, 3, 4
 (FP8MM_SCALE_TENSOR, FP8MM_SCALE_A1x128_B1x128, FP8MM_SCALE_A1x128_B128x128,
- FP8MM_SCALE_MX32_UE8M0) = 0, 1, 2, 3
+ FP8MM_SCALE_MX32_UE8M0, FP8MM_SCALE_NV16_E4M3) = 0, 1, 2, 3, 4
 STATUS = {0: "FP8MM_OK", 1: "FP8MM_ERR_INVALID", 2: "FP8MM_ERR_ALIGNMENT", 3: "FP8MM_ERR_UNSUPPORTED",
           4: "FP8MM_ERR_REJECTED", 5: "FP8MM_ERR_WORKSPACE", 6: "FP8MM_ERR_CUDA", 7: "FP8MM_ERR_DEVICE"}
 FP8MM_OK, FP8MM_ERR_INVALID, FP8MM_ERR_ALIGNMENT, FP8MM_ERR_UNSUPPORTED = 0, 1, 2, 3

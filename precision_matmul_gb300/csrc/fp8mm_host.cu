@@ -24,6 +24,7 @@ struct fp8mm_plan_s {
   int max_smem = 0;
   int swap = 0, bn = 0, splits = 1, kb_per_split = 0, num_kb = 0, stages = 0, num_acc = 2;
   int group = 1, slow = 0, mx = 0, out_es = 4, cg = 1, ew = 8;
+  int f4 = 0, vec16 = 0;  // packed FP4 operands; their factors per 16 (E4M3) rather than per 32 (UE8M0)
   int64_t R = 0, Q = 0;
   int tiles_r = 0, tiles_q = 0;
   long long units = 0;
@@ -115,7 +116,8 @@ cudaError_t ensure_smem_attr(KernelFn fn, int device, size_t bytes) {
 size_t layout(fp8mm_plan_s* P, int stages) {
   const uint32_t x_bytes = kBlockM * kBlockK;
   const uint32_t y_bytes = (uint32_t)(P->bn / P->cg) * kBlockK;
-  const uint32_t sf_bytes = P->mx ? kSfStageBytes : 0u;
+  // FP4: the 4 (per 16) or 2 (per 32) factor atoms of X and of Y per stage
+  const uint32_t sf_bytes = P->f4 ? 2u * (P->vec16 ? 4u : 2u) * 512u : (P->mx ? kSfStageBytes : 0u);
   uint32_t off = 0;
   P->x_stage_bytes = x_bytes;
   P->y_stage_bytes = y_bytes;
@@ -179,11 +181,11 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   *out = nullptr;
   const fp8mm_desc d = *desc;
   if (d.M < 0 || d.N < 0 || d.K < 0 || d.L < 0) return FP8MM_ERR_INVALID;
-  if (d.a_fmt < 0 || d.a_fmt > 1 || d.b_fmt < 0 || d.b_fmt > 1) return FP8MM_ERR_INVALID;
+  if (d.a_fmt < 0 || d.a_fmt > 2 || d.b_fmt < 0 || d.b_fmt > 2) return FP8MM_ERR_INVALID;
   if (d.out_dtype < 0 || d.out_dtype > 4) return FP8MM_ERR_INVALID;
   if (d.bias < 0 || d.bias > 1 || d.a_major < 0 || d.a_major > 1 || d.b_major < 0 || d.b_major > 1)
     return FP8MM_ERR_INVALID;
-  if (d.scale_mode < 0 || d.scale_mode > 3) return FP8MM_ERR_INVALID;
+  if (d.scale_mode < 0 || d.scale_mode > 4) return FP8MM_ERR_INVALID;
   if (d.fast_accum < 0 || d.fast_accum > 1) return FP8MM_ERR_INVALID;
   if (d.splitk < 0 || d.swap_ab < 0 || d.swap_ab > 2 || d.device < 0) return FP8MM_ERR_INVALID;
   if (d.cta_pair < 0 || d.cta_pair > 2) return FP8MM_ERR_INVALID;
@@ -193,6 +195,20 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   if (d.block_n != 0 && !(d.block_n >= 16 && d.block_n <= 256 && d.block_n % 16 == 0)) return FP8MM_ERR_INVALID;
   const int64_t lim = (int64_t)1 << 31;
   if (d.M >= lim || d.N >= lim || d.K >= lim || d.L >= 65536) return FP8MM_ERR_UNSUPPORTED;
+  // Packed FP4 operands (cuDNN "GEMM + Amax (SM100)", Dtypes): A and B both
+  // E2M1, with UE8M0 factors per 32 or E4M3 factors per 16 elements of K,
+  // K-major, fast accumulation; K a multiple of 64 (one MMA's K, and a whole
+  // number of E4M3-factor atoms).
+  const bool f4 = d.a_fmt == FP8MM_E2M1 || d.b_fmt == FP8MM_E2M1;
+  if (f4) {
+    if (d.a_fmt != d.b_fmt) return FP8MM_ERR_UNSUPPORTED;
+    if (d.scale_mode != FP8MM_SCALE_MX32_UE8M0 && d.scale_mode != FP8MM_SCALE_NV16_E4M3) return FP8MM_ERR_UNSUPPORTED;
+    if (!d.fast_accum || d.a_major || d.b_major || d.cta_pair == 1 || d.strict_torch) return FP8MM_ERR_UNSUPPORTED;
+    if (d.block_n != 0 && d.block_n != 128) return FP8MM_ERR_UNSUPPORTED;
+    if (d.K % 64 != 0) return FP8MM_ERR_ALIGNMENT;
+  } else if (d.scale_mode == FP8MM_SCALE_NV16_E4M3) {
+    return FP8MM_ERR_UNSUPPORTED;  // factors per 16 elements go with FP4 operands only
+  }
   if (d.K % 16 != 0) return FP8MM_ERR_ALIGNMENT;
   if ((d.N * out_size(d.out_dtype)) % 16 != 0) return FP8MM_ERR_ALIGNMENT;
   // M/N-major operands: their rows ([K][M] or [K][N] bytes) must be 16-byte multiples
@@ -200,7 +216,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   const bool fp8_out = d.out_dtype == FP8MM_OUT_E4M3 || d.out_dtype == FP8MM_OUT_E5M2;
   // the pages define a bias for bf16 / fp16 (and here fp32) outputs only
   if (d.bias && fp8_out) return FP8MM_ERR_UNSUPPORTED;
-  const bool mx = d.scale_mode == FP8MM_SCALE_MX32_UE8M0;
+  const bool mx = d.scale_mode == FP8MM_SCALE_MX32_UE8M0 || d.scale_mode == FP8MM_SCALE_NV16_E4M3;
   if (mx && d.a_fmt != d.b_fmt) return FP8MM_ERR_UNSUPPORTED;
   // torch._scaled_mm refuses E5M2 x E5M2; the library computes it unless the
   // caller asks for torch's refusals.
@@ -226,6 +242,8 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
     return FP8MM_ERR_CUDA;
   }
   P->mx = mx ? 1 : 0;
+  P->f4 = f4 ? 1 : 0;
+  P->vec16 = d.scale_mode == FP8MM_SCALE_NV16_E4M3 ? 1 : 0;
   P->out_es = out_size(d.out_dtype);
   const bool blockwise = d.scale_mode == FP8MM_SCALE_A1x128_B1x128 || d.scale_mode == FP8MM_SCALE_A1x128_B128x128;
   P->slow = (blockwise || !d.fast_accum) ? 1 : 0;
@@ -252,14 +270,15 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
       P->y_kind = kScaleRow;
     }
   }
-  P->num_kb = (int)cdiv(d.K, kBlockK);
+  // a stage holds 128 bytes of K per row: 128 FP8 or 256 FP4 elements
+  P->num_kb = (int)cdiv(d.K, f4 ? 2 * kBlockK : kBlockK);
   const int64_t L = std::max<int64_t>(1, d.L);
   const int64_t tiles_r1 = std::max<int64_t>(1, cdiv(P->R, kBlockM));
 
   // Tile width on the MMA's N side.  Wide problems pick the width whose
   // whole waves over the SMs cost least; narrow ones the smallest
   // power-of-two width that covers Q.
-  int bn = d.block_n;
+  int bn = f4 ? 128 : d.block_n;
   // Two-SM pair tiles (256 rows, cta_group::2): each SM stages half as many
   // Y bytes per MMA, which measured 4-15% faster than single-CTA tiles on
   // GB300 for fast unswapped GEMMs with at least one wave of pairs.
@@ -347,7 +366,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   const bool wide = wide_slow(bn, P->slow != 0);
   const bool wide_ycol = wide && blockwise && P->y_kind == kScaleRow;
   P->ew = d.epi_warps ? d.epi_warps : ((P->slow && !mx && bn == 128 && P->cg == 1) ? 16 : 8);
-  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew);
+  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew, f4);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
   if (device_checks && held_tile(bn, P->slow != 0, mx)) {
     // The warpgroup register split only redistributes what the block was
@@ -419,7 +438,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // to three chunks ahead of the promotion.
   P->num_acc = (P->slow && !mx && 4 * bn <= 512) ? 4 : 2;
   if (mx) {
-    const int tmem_stages = (512 - 2 * bn) / 16;
+    const int tmem_stages = (512 - 2 * bn) / (f4 ? 8 * (P->vec16 ? 4 : 2) : 16);
     if (tmem_stages >= 3)
       stages = std::min(stages, tmem_stages);
     else
@@ -430,7 +449,8 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   P->stages = stages;
   P->smem_bytes = layout(P, stages);
   if (P->smem_bytes > (size_t)P->max_smem) return FP8MM_ERR_UNSUPPORTED;
-  const uint32_t need = (uint32_t)(P->num_acc * bn) + (mx ? 16u * (uint32_t)stages : 0u);
+  const uint32_t sf_cols = f4 ? 8u * (P->vec16 ? 4u : 2u) : 16u;  // TMEM columns of one stage's factors
+  const uint32_t need = (uint32_t)(P->num_acc * bn) + (mx ? sf_cols * (uint32_t)stages : 0u);
   uint32_t cols = 32;
   while (cols < need) cols *= 2;
   if (cols > 512) return FP8MM_ERR_UNSUPPORTED;
@@ -514,12 +534,17 @@ fp8mm_status fp8mm_plan_roofline(const fp8mm_plan_t* plan, double* flops, double
     case FP8MM_SCALE_A1x128_B1x128: sbytes = 4.0 * L * (M + N) * kb; break;
     case FP8MM_SCALE_A1x128_B128x128: sbytes = 4.0 * L * (M + (double)cdiv(d.N, 128)) * kb; break;
     case FP8MM_SCALE_MX32_UE8M0:
-      sbytes = 512.0 * L * kb * (double)(cdiv(d.M, 128) + cdiv(d.N, 128));
+    case FP8MM_SCALE_NV16_E4M3: {
+      // one 512-byte atom per 128 rows and 4 factors along K
+      const double atoms_k = (double)cdiv(d.K, 4 * (d.scale_mode == FP8MM_SCALE_NV16_E4M3 ? 16 : 32));
+      sbytes = 512.0 * L * atoms_k * (double)(cdiv(d.M, 128) + cdiv(d.N, 128));
       break;
+    }
     default: break;
   }
+  const double opb = plan->f4 ? 0.5 : 1.0;  // operand bytes per element
   *flops = 2.0 * L * M * N * K;
-  *bytes = L * (M * K + N * K) + sbytes + (d.bias ? N * (double)plan->out_es : 0.0) +
+  *bytes = opb * L * (M * K + N * K) + sbytes + (d.bias ? N * (double)plan->out_es : 0.0) +
            L * M * N * (double)plan->out_es + 4.0;
   return FP8MM_OK;
 }
@@ -646,9 +671,10 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
   const void* xptr = P->swap ? b : a;
   const void* yptr = P->swap ? a : b;
   CUtensorMap tm_x, tm_y, tm_c;
+  const int64_t kbytes = P->f4 ? d.K / 2 : d.K;  // bytes of K per operand row (FP4: two elements per byte)
   {
-    cuuint64_t dims[3] = {(cuuint64_t)d.K, (cuuint64_t)P->R, (cuuint64_t)d.L};
-    cuuint64_t strides[2] = {(cuuint64_t)d.K, (cuuint64_t)(d.K * P->R)};
+    cuuint64_t dims[3] = {(cuuint64_t)kbytes, (cuuint64_t)P->R, (cuuint64_t)d.L};
+    cuuint64_t strides[2] = {(cuuint64_t)kbytes, (cuuint64_t)(kbytes * P->R)};
     cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)kBlockM, 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(xptr), dims, strides, box, es,
@@ -657,8 +683,8 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
       return FP8MM_ERR_CUDA;
   }
   {
-    cuuint64_t dims[3] = {(cuuint64_t)d.K, (cuuint64_t)P->Q, (cuuint64_t)d.L};
-    cuuint64_t strides[2] = {(cuuint64_t)d.K, (cuuint64_t)(d.K * P->Q)};
+    cuuint64_t dims[3] = {(cuuint64_t)kbytes, (cuuint64_t)P->Q, (cuuint64_t)d.L};
+    cuuint64_t strides[2] = {(cuuint64_t)kbytes, (cuuint64_t)(kbytes * P->Q)};
     cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)(P->bn / P->cg), 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(&tm_y, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(yptr), dims, strides, box, es,
@@ -725,7 +751,13 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
   kp.tmem_cols = P->tmem_cols;
   const uint32_t xf = (uint32_t)(P->swap ? d.b_fmt : d.a_fmt);
   const uint32_t yf = (uint32_t)(P->swap ? d.a_fmt : d.b_fmt);
-  if (P->mx) {
+  if (P->f4) {
+    // kind::mxf4nvf4: E2M1 operands (format code 1 at bits 7-9 and 10-12), N>>3 at 17, scale type
+    // at bit 23 (1 UE8M0 factors per 32 elements, 0 E4M3 factors per 16), M>>4 at 24; the
+    // scale-factor ids of the 2X form are added per MMA in the kernel.
+    kp.idesc = (1u << 7) | (1u << 10) | ((uint32_t)(P->bn >> 3) << 17) | ((P->vec16 ? 0u : 1u) << 23) |
+               ((uint32_t)(kBlockM >> 4) << 24);
+  } else if (P->mx) {
     // kind::mxf8f6f4: B scale id bits 4-5, formats 7-9 / 10-12, N>>3 at 17, UE8M0 scale type bit 23,
     // M>>4 at 24, A scale id bits 29-30 (ids added per K step in the kernel).
     kp.idesc = (xf << 7) | (yf << 10) | ((uint32_t)(P->bn >> 3) << 17) | (1u << 23) |
@@ -747,7 +779,8 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
     kp.x_kind = P->x_kind;
     kp.y_kind = P->y_kind;
   }
-  kp.scale_kb = P->num_kb;
+  kp.scale_kb = P->f4 ? (int)cdiv(d.K, 4 * (P->vec16 ? 16 : 32)) : P->num_kb;
+  kp.f4_vec16 = P->vec16;
   kp.sfx_mb = (int)cdiv(P->R, 128);
   kp.sfy_mb = (int)cdiv(P->Q, 128);
   kp.amax_bits = reinterpret_cast<unsigned*>(amax);
@@ -770,7 +803,7 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
   kp.out_swz_mask = swz_mask;
   kp.out_rowbytes = rowbytes;
 
-  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew);
+  KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew, P->f4 != 0);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
   if (ensure_smem_attr(fn, d.device, (size_t)P->max_smem) != cudaSuccess) return FP8MM_ERR_CUDA;
   void* args[4] = {&tm_x, &tm_y, &tm_c, &kp};

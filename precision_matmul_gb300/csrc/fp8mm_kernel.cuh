@@ -138,9 +138,11 @@ struct KParams {
   int x_kind;
   const float* y_scale;
   int y_kind;
-  int scale_kb;           // ceil(K / 128): row stride of the block-scale arrays and atom count along K
+  int scale_kb;           // block scales: ceil(K / 128), the row stride of the scale arrays; factor
+                          // atoms: their count along K (ceil(K / 128) for FP8, ceil(K / (4 vec)) for FP4)
   const uint8_t* sfx;     // MX scale-factor atoms of X and Y
   const uint8_t* sfy;
+  int f4_vec16;           // FP4 operands: 1 E4M3 factors per 16 elements (4X), 0 UE8M0 per 32 (2X)
   int sfx_mb, sfy_mb;     // ceil(R / 128), ceil(Q / 128)
   float* ws_partials;     // split-K partial tiles [tile][split][col][row]
   unsigned* ws_counters;  // split-K arrivals per tile
@@ -756,10 +758,15 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   if (lane == 0 && amax_local != 0u) atomicMax(p.amax_bits, amax_local);
 }
 
-template <int BN, bool SLOW, bool MX, int CG, int EW>
+// F4: packed FP4 (E2M1) operands with block scaling (kind::mxf4nvf4): a stage
+// row of 128 bytes holds 256 elements, four MMAs of K = 64; each stage brings
+// the 4 (E4M3 per 16) or 2 (UE8M0 per 32) factor atoms of X and of Y that
+// cover its 256 elements.
+template <int BN, bool SLOW, bool MX, int CG, int EW, bool F4 = false>
 __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1)
     fp8mm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                  const __grid_constant__ CUtensorMap tm_c, const KParams p) {
+  static_assert(!F4 || (MX && BN == 128 && !SLOW && CG == 1), "FP4: 128-column block-scaled tiles, fast");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(!MX || BN == 128 || BN == 256 || (BN % 32 == 0 && BN < 256),
                 "MX tiles start on a 32-row boundary of a factor atom");
@@ -869,8 +876,12 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
         // MX: Y's tile may start inside a 128-row atom; copy every atom it touches.
         const int y_atom0 = (t.tq * BN) / 128;
         const int y_atoms = (MX && !GATHER) ? ((t.tq * BN) % 128 + BN + 127) / 128 : 0;
-        const uint32_t tx = CG * (p.x_stage_bytes + p.y_stage_bytes) + (MX ? 512u * (1 + y_atoms) : 0u);
+        const uint32_t tx0 = CG * (p.x_stage_bytes + p.y_stage_bytes) + ((MX && !F4) ? 512u * (1 + y_atoms) : 0u);
+        const int apk = p.f4_vec16 ? 4 : 2;  // FP4: factor atoms per stage and operand
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          // FP4: the atoms that exist for this stage's 256 elements of K
+          const int f4_na = F4 ? min(apk, p.scale_kb - kb * apk) : 0;
+          const uint32_t tx = tx0 + (F4 ? 1024u * (uint32_t)f4_na : 0u);
           {
             bool w = wait_bar(bar_empty + 8u * stage, phase ^ 1u, abort_flag, p.abort_word, kErrProducer);
             if constexpr (GATHER) w = __all_sync(0xFFFFFFFFu, w);  // the lanes leave together
@@ -893,7 +904,16 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
             ptx::tma_load_3d(sbase + p.off_x + stage * p.x_stage_bytes, &tm_x, fb, kb * kBlockK, xrow0, t.l);
             ptx::tma_load_3d(sbase + p.off_y + stage * p.y_stage_bytes, &tm_y, fb, kb * kBlockK, yrow0, t.l);
           }
-          if constexpr (MX) {
+          if constexpr (F4) {
+            // X atoms in slots 0 .. apk-1, Y atoms in slots apk .. 2 apk-1
+            const uint32_t sf = sbase + p.off_sf + stage * p.sf_stage_bytes;
+            for (int i = 0; i < f4_na; ++i) {
+              const size_t a = (size_t)kb * apk + i;
+              ptx::bulk_load(sf + 512u * i, p.sfx + (((size_t)t.l * p.sfx_mb + t.tr) * p.scale_kb + a) * 512u, 512u, fb);
+              ptx::bulk_load(sf + 512u * (apk + i), p.sfy + (((size_t)t.l * p.sfy_mb + t.tq) * p.scale_kb + a) * 512u,
+                             512u, fb);
+            }
+          } else if constexpr (MX) {
             const uint32_t sf = sbase + p.off_sf + stage * p.sf_stage_bytes;
             const uint8_t* gx =
                 p.sfx + (((size_t)t.l * p.sfx_mb + t.tr) * p.scale_kb + kb) * 512u;
@@ -969,7 +989,32 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
           const uint32_t d = tmem_base + abuf * BN;
           const uint64_t adesc = ptx::desc_sw128_kmajor(sbase + p.off_x + stage * p.x_stage_bytes);
           const uint64_t bdesc = ptx::desc_sw128_kmajor(sbase + p.off_y + stage * p.y_stage_bytes);
-          if constexpr (MX) {
+          if constexpr (F4) {
+            // TMEM slot of 8 apk columns per stage: X's atoms, then Y's, 4 columns each.
+            const int apk = p.f4_vec16 ? 4 : 2;
+            const int na = min(apk, p.scale_kb - kb * apk);
+            const uint32_t sf_smem = sbase + p.off_sf + stage * p.sf_stage_bytes;
+            const uint32_t sf_x = tmem_base + (uint32_t)(p.num_acc * BN) + stage * (uint32_t)(8 * apk);
+            const uint32_t sf_y = sf_x + 4u * (uint32_t)apk;
+            for (int i = 0; i < na; ++i) {
+              ptx::tmem_cp_32x128b_warpx4(sf_x + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * i));
+              ptx::tmem_cp_32x128b_warpx4(sf_y + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * (apk + i)));
+            }
+#pragma unroll
+            for (int k = 0; k < kBlockK / 32; ++k) {
+              // an MMA of K = 64 elements (32 bytes); none past the end of K
+              if (kb * 256 + 64 * k >= p.K) break;
+              const uint32_t acc = (!gstart || k > 0) ? 1u : 0u;
+              if (p.f4_vec16) {
+                ptx::mma_mxf4nvf4_4x(d, adesc + 2u * k, bdesc + 2u * k, p.idesc, sf_x + 4u * k, sf_y + 4u * k, acc);
+              } else {
+                // the atom holds 4 factors per row: MMA k reads bytes 2 (k % 2) .. +1 of atom k / 2
+                const uint32_t id = (uint32_t)(k & 1) * 2u;
+                ptx::mma_mxf4nvf4_2x(d, adesc + 2u * k, bdesc + 2u * k, p.idesc | (id << 29) | (id << 4),
+                                     sf_x + 4u * (k >> 1), sf_y + 4u * (k >> 1), acc);
+              }
+            }
+          } else if constexpr (MX) {
             const uint32_t sf_smem = sbase + p.off_sf + stage * p.sf_stage_bytes;
             const uint32_t sf_x = tmem_base + (uint32_t)(p.num_acc * BN) + stage * 16u;
             // TMEM slot of 16 columns per stage: X's atom in columns 0-3, Y's

@@ -22,9 +22,9 @@ import dataclasses
 
 import torch
 
-E4M3, E5M2 = 0, 1
+E4M3, E5M2, E2M1 = 0, 1, 2
 OUT_F32, OUT_BF16, OUT_F16, OUT_E4M3, OUT_E5M2 = 0, 1, 2, 3, 4
-SCALE_TENSOR, SCALE_A1x128_B1x128, SCALE_A1x128_B128x128, SCALE_MX32_UE8M0 = 0, 1, 2, 3
+SCALE_TENSOR, SCALE_A1x128_B1x128, SCALE_A1x128_B128x128, SCALE_MX32_UE8M0, SCALE_NV16_E4M3 = 0, 1, 2, 3, 4
 
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 TORCH_FP8 = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
@@ -37,7 +37,8 @@ OUT_NAME = {OUT_F32: "f32", OUT_BF16: "bf16", OUT_F16: "f16", OUT_E4M3: "e4m3", 
 class Problem:
     """One GEMM call's inputs, on the CPU.
 
-    a: uint8 codes [L][M][K]; b: uint8 codes [L][N][K] (both K-innermost).
+    a: uint8 codes [L][M][K]; b: uint8 codes [L][N][K] (both K-innermost; packed
+    FP4 operands hold K/2 bytes per row).
     scale_a / scale_b: float32 (per-tensor: shape [1]; 1x128: [L][rows][ceil(K/128)];
     128x128: [L][ceil(N/128)][ceil(K/128)]) or uint8 UE8M0 atoms for the MX form
     (physical layout [L][ceil(rows/128)][ceil(K/128)][32][4][4]).
@@ -139,6 +140,53 @@ def _mx_factors(g: torch.Generator, L: int, R: int, K: int, lo=-6, hi=6) -> torc
     """UE8M0 codes 127 + U{lo..hi}, physical atom layout [L][R/128][K/128][32][4][4]."""
     shape = (L, (R + 127) // 128, _kb(K), 32, 4, 4)
     return (torch.randint(lo, hi + 1, shape, generator=g) + 127).to(torch.uint8)
+
+
+# E2M1 (FP4) magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes 0..7) and the midpoints between them.
+_E2M1_MIDS = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+
+
+def cast_e2m1(x: torch.Tensor) -> torch.Tensor:
+    """float32 -> E2M1 codes (one per element, low four bits): round to nearest,
+    ties to the even code, saturate at 6; bit 3 is the sign."""
+    mag = x.abs().clamp(max=6.0)
+    code = torch.bucketize(mag, _E2M1_MIDS)            # midpoints strictly below mag
+    tie = (mag == _E2M1_MIDS[code.clamp(max=6)]) & (code % 2 == 1)
+    code = code + tie.to(code.dtype)
+    return (code | (torch.signbit(x).to(code.dtype) << 3)).to(torch.uint8)
+
+
+def pack_fp4(codes: torch.Tensor) -> torch.Tensor:
+    """Two E2M1 codes per byte along the last dimension: element 2i in the low
+    four bits of byte i, element 2i + 1 in the high four bits."""
+    return (codes[..., 0::2] | (codes[..., 1::2] << 4)).contiguous()
+
+
+def fp4_batched(L=4, M=4096, N=4096, K=4096, form="nv16", seed=7, out_dtype=OUT_F32) -> Problem:
+    """Block-scaled FP4 batched GEMM (cuDNN "GEMM + Amax (SM100)", float4_e2m1fn_x2
+    operands): per block of 16 (NVFP4, positive E4M3 factors 0.25 .. 4) or 32
+    (MXFP4, UE8M0 factors 2^-6 .. 2^6) elements along K, x ~ N(0,1),
+    q = cast_e2m1(x * 6 / max|x_blk|); a and b packed, [L][rows][K/2]."""
+    vec = 16 if form == "nv16" else 32
+    g = _gen(seed)
+
+    def operand(R):
+        Kp = (K + vec - 1) // vec * vec
+        x = torch.randn(L, R, Kp, generator=g)
+        blk = x.view(L, R, Kp // vec, vec)
+        mx = blk.abs().amax(dim=-1, keepdim=True).clamp_min(1e-30)
+        return pack_fp4(cast_e2m1((blk * (6.0 / mx)).view(L, R, Kp)[:, :, :K]))
+
+    def factors(R):
+        shape = (L, (R + 127) // 128, (K + 4 * vec - 1) // (4 * vec), 32, 4, 4)
+        if vec == 16:
+            return torch.randint(0x28, 0x49, shape, generator=g).to(torch.uint8)  # E4M3 0.25 .. 4
+        return (torch.randint(-6, 7, shape, generator=g) + 127).to(torch.uint8)
+
+    a, b = operand(M), operand(N)
+    sfa, sfb = factors(M), factors(N)
+    mode = SCALE_NV16_E4M3 if vec == 16 else SCALE_MX32_UE8M0
+    return Problem(f"fp4_{form}", L, M, N, K, a, b, sfa, sfb, E2M1, E2M1, mode, out_dtype, True)
 
 
 def mx_batched(L=4, M=4096, N=4096, K=4096, fmt=E4M3, seed=3, out_dtype=OUT_F32) -> Problem:

@@ -103,7 +103,14 @@ def _plan_status(**kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(M=-1, N=16, K=16), B.FP8MM_ERR_INVALID),
-    (dict(M=16, N=16, K=16, a_fmt=2), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, a_fmt=3), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=64, a_fmt=2, scale_mode=3), B.FP8MM_ERR_UNSUPPORTED),          # FP4 x FP8
+    (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=0), B.FP8MM_ERR_UNSUPPORTED),  # FP4 needs factors
+    (dict(M=16, N=16, K=32, a_fmt=2, b_fmt=2, scale_mode=4), B.FP8MM_ERR_ALIGNMENT),    # K % 64
+    (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=4, fast_accum=0), B.FP8MM_ERR_UNSUPPORTED),
+    (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=4, block_n=256), B.FP8MM_ERR_UNSUPPORTED),
+    (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=4), B.FP8MM_OK),
+    (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=3), B.FP8MM_OK),
     (dict(M=16, N=16, K=16, out_dtype=5), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, bias=2), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, a_major=2), B.FP8MM_ERR_INVALID),
@@ -114,7 +121,8 @@ def _plan_status(**kw):
     (dict(M=16, N=16, K=16, out_dtype=4, strict_torch=1), B.FP8MM_ERR_REJECTED),  # E4M3 x E4M3 -> E5M2
     (dict(M=16, N=16, K=16, out_dtype=4), B.FP8MM_OK),
     (dict(M=16, N=16, K=16, out_dtype=3, a_major=1, b_major=1, bias=0), B.FP8MM_OK),
-    (dict(M=16, N=16, K=16, scale_mode=4), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, scale_mode=5), B.FP8MM_ERR_INVALID),
+    (dict(M=16, N=16, K=16, scale_mode=4), B.FP8MM_ERR_UNSUPPORTED),   # per-16 factors with FP8 operands
     (dict(M=16, N=16, K=16, fast_accum=2), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, block_n=40), B.FP8MM_ERR_INVALID),
     (dict(M=16, N=16, K=16, epi_warps=12), B.FP8MM_ERR_INVALID),
