@@ -64,3 +64,35 @@ def test_static_workspace_refuses_oversized_plans():
         B.fp8mm_run_static_workspace(plan, 16, 16, 16, 16, 16, 16, None)
     assert e.value.status == B.FP8MM_ERR_WORKSPACE
     np.testing.assert_equal(B.fp8mm_device_error(0), 0)
+
+
+def test_static_workspace_slow_block_scaled_split_k_swapped():
+    # the promoted (slow) path of a block-scaled, swapped, split-K plan: partial
+    # tiles of promoted sums go through the library's array instead of a caller buffer
+    dev = torch.device("cuda:0")
+    p = synth.blockwise(M=48, N=1024, K=2048, seed=104)
+    d = _desc_for(p)
+    d.splitk, d.swap_ab = 3, 1
+    plan = B.Plan(d)
+    info = plan.info()
+    ws_bytes = plan.workspace_size()
+    assert info["slow"] == 1 and info["swap_ab"] == 1 and info["splitk"] == 3
+    assert 0 < ws_bytes <= B.FP8MM_STATIC_WORKSPACE_BYTES
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    a, b = p.a[0].to(dev), p.b[0].to(dev)
+    sa, sb = p.scale_a.to(dev), p.scale_b.to(dev)
+    c_ref = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
+    m_ref = torch.empty(1, dtype=torch.float32, device=dev)
+    B.fp8mm_run(plan, a.data_ptr(), b.data_ptr(), sa.data_ptr(), sb.data_ptr(), c_ref.data_ptr(),
+                m_ref.data_ptr(), ws.data_ptr(), ws_bytes, stream)
+    for _ in range(2):
+        c = torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device=dev)
+        m = torch.full((1,), -1.0, dtype=torch.float32, device=dev)
+        B.fp8mm_run_static_workspace(plan, a.data_ptr(), b.data_ptr(), sa.data_ptr(), sb.data_ptr(),
+                                     c.data_ptr(), m.data_ptr(), stream)
+        torch.cuda.synchronize()
+        assert B.fp8mm_device_error(0) == 0
+        assert torch.equal(c.view(torch.int16), c_ref.view(torch.int16))
+        assert torch.equal(m.view(torch.int32), m_ref.view(torch.int32))
+        check(p, c, m)
