@@ -590,7 +590,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         v, cores, sample = oracle_sample(probs, target_s=args.cpu_seconds)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
-    fmts = sorted({("fp8_e4m3" if p.a_fmt == 0 else "fp8_e5m2") for _, _, p in probs})
+    fmts = sorted({{0: "fp8_e4m3", 1: "fp8_e5m2", 2: "fp4_e2m1"}[p.a_fmt] for _, _, p in probs})
     cfg = config_of(args.workload, probs)
     cfg.update({"l2": "L2 flushed before every timed GEMM: 256 MiB written, then read back (not timed)",
                 "parallelism": f"replicas x{world}"})

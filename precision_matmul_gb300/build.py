@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfp8mm.so")
 SOURCES = ["fp8mm_host.cu", "fp8mm_aux.cu", "fp8mm_inst_narrow.cu", "fp8mm_inst_fast128.cu", "fp8mm_inst_fast256.cu",
-           "fp8mm_inst_pair.cu", "fp8mm_inst_slow.cu", "fp8mm_inst_slow_wide.cu", "fp8mm_inst_slow_pair.cu", "fp8mm_inst_mx.cu", "fp8mm_inst_mx_wide.cu",
+           "fp8mm_inst_pair.cu", "fp8mm_inst_slow.cu", "fp8mm_inst_slow_wide.cu", "fp8mm_inst_slow_pair.cu", "fp8mm_inst_slow_held.cu", "fp8mm_inst_mx.cu", "fp8mm_inst_mx_wide.cu",
            "fp8mm_inst_f4.cu"]
 HEADERS = ["fp8mm_kernel.cuh", "fp8mm_kernels.h", "ptx.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

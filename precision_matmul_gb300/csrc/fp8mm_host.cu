@@ -31,7 +31,7 @@ struct fp8mm_plan_s {
   int grid = 0;
   uint32_t tmem_cols = 0;
   int x_kind = kScaleNone, y_kind = kScaleNone;
-  uint32_t off_x = 0, off_y = 0, off_sf = 0, off_out = 0, off_ys = 0, off_bar = 0;
+  uint32_t off_x = 0, off_y = 0, off_sf = 0, off_out = 0, off_ys = 0, off_bias = 0, off_bar = 0;
   uint32_t x_stage_bytes = 0, y_stage_bytes = 0, sf_stage_bytes = 0;
   size_t smem_bytes = 0;
   size_t ws_partials_bytes = 0, ws_counters_off = 0, ws_counters_bytes = 0, ws_bytes = 0;
@@ -117,7 +117,8 @@ size_t layout(fp8mm_plan_s* P, int stages) {
   const uint32_t x_bytes = kBlockM * kBlockK;
   const uint32_t y_bytes = (uint32_t)(P->bn / P->cg) * kBlockK;
   // FP4: the 4 (per 16) or 2 (per 32) factor atoms of X and of Y per stage
-  const uint32_t sf_bytes = P->f4 ? 2u * (P->vec16 ? 4u : 2u) * 512u : (P->mx ? kSfStageBytes : 0u);
+  const uint32_t sf_bytes = P->f4 ? (1u + (uint32_t)P->bn / 128u) * (P->vec16 ? 4u : 2u) * 512u
+                                  : (P->mx ? kSfStageBytes : 0u);
   uint32_t off = 0;
   P->x_stage_bytes = x_bytes;
   P->y_stage_bytes = y_bytes;
@@ -135,6 +136,10 @@ size_t layout(fp8mm_plan_s* P, int stages) {
   P->off_ys = off;
   // per-column Y scales of the current chunk, one row per epilogue warp
   if (P->x_kind != kScaleNone && P->y_kind == kScaleRow) off += (uint32_t)(P->ew * part_max_cols(P->bn, P->ew, P->slow != 0) * 4);
+  off = (off + 127u) & ~127u;
+  P->off_bias = off;
+  // the bias of each epilogue warp's columns (fp32), staged once per tile
+  if (P->d.bias) off += (uint32_t)(P->ew * part_max_cols(P->bn, P->ew, P->slow != 0) * 4);
   off = (off + 127u) & ~127u;
   P->off_bar = off;
   off += 16u * stages + 80u + 16u;  // full/empty per stage, 4+4 accumulator barriers, epilogue, drain, misc
@@ -204,7 +209,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
     if (d.a_fmt != d.b_fmt) return FP8MM_ERR_UNSUPPORTED;
     if (d.scale_mode != FP8MM_SCALE_MX32_UE8M0 && d.scale_mode != FP8MM_SCALE_NV16_E4M3) return FP8MM_ERR_UNSUPPORTED;
     if (!d.fast_accum || d.a_major || d.b_major || d.cta_pair == 1 || d.strict_torch) return FP8MM_ERR_UNSUPPORTED;
-    if (d.block_n != 0 && d.block_n != 128) return FP8MM_ERR_UNSUPPORTED;
+    if (d.block_n != 0 && d.block_n != 128 && d.block_n != 256) return FP8MM_ERR_UNSUPPORTED;
     if (d.K % 64 != 0) return FP8MM_ERR_ALIGNMENT;
   } else if (d.scale_mode == FP8MM_SCALE_NV16_E4M3) {
     return FP8MM_ERR_UNSUPPORTED;  // factors per 16 elements go with FP4 operands only
@@ -278,7 +283,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // Tile width on the MMA's N side.  Wide problems pick the width whose
   // whole waves over the SMs cost least; narrow ones the smallest
   // power-of-two width that covers Q.
-  int bn = f4 ? 128 : d.block_n;
+  int bn = d.block_n;
   // Two-SM pair tiles (256 rows, cta_group::2): each SM stages half as many
   // Y bytes per MMA, which measured 4-15% faster than single-CTA tiles on
   // GB300 for fast unswapped GEMMs with at least one wave of pairs.
@@ -317,14 +322,30 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
       // Skinny problems stream X (the long operand) from HBM once; the whole
       // of Y fits one tile and split-K fills the waves.
     } else if (P->slow && P->Q > 128) {
-      // Slow accumulation: 256 columns (full-rate MMAs, never split) when
-      // they fill the SMs, else 128 (split-K can fill the waves).
-      bn = (!mx && d.splitk <= 1 && tiles_r1 * cdiv(P->Q, 256) * L >= (int64_t)P->sms) ? 256 : 128;
+      // Slow accumulation: held tiles of 192-256 columns (never split) when
+      // they fill the SMs, else 128 (split-K can fill the waves).  A held
+      // chunk's time follows its operand bytes (128 rows of X and BN of Y,
+      // 128 bytes of K each), so the width with the fewest whole waves x
+      // bytes per chunk wins; 128x128 Y scales need 128-aligned halves (256).
+      bn = 128;
+      if (!mx && d.splitk <= 1 && tiles_r1 * cdiv(P->Q, 256) * L >= (int64_t)P->sms) {
+        double best = 1e300;
+        for (int c : {256, 224, 192}) {
+          if (c != 256 && y_block128) continue;
+          const int64_t tiles = tiles_r1 * cdiv(P->Q, c) * L;
+          const double cost = (double)cdiv(tiles, P->sms) * (kBlockM + c);
+          if (cost < best * 0.999) {
+            best = cost;
+            bn = c;
+          }
+        }
+      }
     } else if (!P->slow && P->Q > 128 && tiles_r1 * cdiv(P->Q, 256) * L > (int64_t)P->sms) {
       // (under one wave of 256-wide tiles the widest tile is the fastest)
       double best = 1e300;
       for (int c : {256, 224, 192, 128}) {
         if (mx && c == 192) continue;
+        if (f4 && c == 224) continue;  // FP4 tiles are 128 or 256 columns
         const int64_t tiles = tiles_r1 * cdiv(P->Q, c) * L;
         const double cost = (double)cdiv(tiles, P->sms) * c / width_efficiency(c, mx);
         if (cost < best * 0.999) {
@@ -334,11 +355,12 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
       }
     }
   }
-  // Slow accumulation keeps the promoted sums in registers: 256 columns on one
-  // CTA or a CTA pair, 224 on a CTA pair only, never swapped, split or MX.
+  // Slow accumulation keeps the promoted sums in registers: 192, 224 or 256
+  // columns on one CTA (224 and 256 on a CTA pair too), never swapped, split
+  // or MX; 192/224 only where no 128x128 Y-scale block straddles a half.
   const bool pair = d.cta_pair == 1 || auto_pair;
   const bool slow_wide_ok = !swap && !mx && d.splitk <= 1 &&
-                            (bn == 256 || (bn == 224 && pair && !y_block128));
+                            (bn == 256 || ((bn == 224 || (bn == 192 && !pair)) && !y_block128));
   if (P->slow && bn > 128 && !slow_wide_ok) {
     if (d.block_n != 0) return FP8MM_ERR_UNSUPPORTED;
     bn = 128;
@@ -349,6 +371,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // factors from a TMEM column aligned to an atom's four columns, so the
   // 224-column kernel gathers Y's factor atoms to start at the tile's first row.
   if (mx && bn != 128 && bn != 224 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
+  if (f4 && bn != 128 && bn != 256) return FP8MM_ERR_UNSUPPORTED;
   // FP8 outputs are stored in rows of at least 16 bytes that start on 16-byte
   // columns: unswapped tiles of 16 columns (8 per epilogue warp) are too narrow.
   if (fp8_out && !swap && bn < 32) {
@@ -437,19 +460,22 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // tiles four chunk buffers fill the 512 TMEM columns and let the MMA run up
   // to three chunks ahead of the promotion.
   P->num_acc = (P->slow && !mx && 4 * bn <= 512) ? 4 : 2;
+  // TMEM columns of one stage's factors (block-scaled forms)
+  const uint32_t sf_cols = f4 ? 4u * (P->vec16 ? 4u : 2u) * (1u + (uint32_t)bn / 128u) : 16u;
   if (mx) {
-    const int tmem_stages = (512 - 2 * bn) / (f4 ? 8 * (P->vec16 ? 4 : 2) : 16);
-    if (tmem_stages >= 3)
+    const int tmem_stages = (512 - 2 * bn) / (int)sf_cols;
+    if (tmem_stages >= 3) {
       stages = std::min(stages, tmem_stages);
-    else
+    } else {
       P->num_acc = 1;
+      stages = std::min(stages, (512 - bn) / (int)sf_cols);
+    }
   } else if (2 * bn > 512) {
     P->num_acc = 1;
   }
   P->stages = stages;
   P->smem_bytes = layout(P, stages);
   if (P->smem_bytes > (size_t)P->max_smem) return FP8MM_ERR_UNSUPPORTED;
-  const uint32_t sf_cols = f4 ? 8u * (P->vec16 ? 4u : 2u) : 16u;  // TMEM columns of one stage's factors
   const uint32_t need = (uint32_t)(P->num_acc * bn) + (mx ? sf_cols * (uint32_t)stages : 0u);
   uint32_t cols = 32;
   while (cols < need) cols *= 2;
@@ -796,6 +822,7 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
   kp.off_sf = P->off_sf;
   kp.off_out = P->off_out;
   kp.off_ys = P->off_ys;
+  kp.off_bias = P->off_bias;
   kp.off_bar = P->off_bar;
   kp.x_stage_bytes = P->x_stage_bytes;
   kp.y_stage_bytes = P->y_stage_bytes;

@@ -4,5 +4,6 @@
 namespace fp8mm {
 
 KernelFn kernel_bn128_fast_f4_cg1_ew8() { return &fp8mm_kernel<128, false, true, 1, 8, true>; }
+KernelFn kernel_bn256_fast_f4_cg1_ew8() { return &fp8mm_kernel<256, false, true, 1, 8, true>; }
 
 }  // namespace fp8mm

@@ -69,9 +69,9 @@ static_assert(2 * epi_regs(8) + kRegRoles <= 512 && 4 * epi_regs(16) + kRegRoles
 static_assert((8 * epi_regs(8) + 4 * kRegRoles) <= 12 * launch_regs(8) &&
                   (16 * epi_regs(16) + 4 * kRegRoles) <= 20 * launch_regs(16),
               "register split within the launch's allocation");
-// Slow accumulation on 224- and 256-column tiles: each epilogue warp keeps 112
-// or 128 (8 warps) or 64 (16 warps, 256 columns) promoted fp32 sums per row in
-// registers.
+// Slow accumulation on 192-, 224- and 256-column tiles: each epilogue warp
+// keeps 96, 112 or 128 (8 warps) or 64 (16 warps, 256 columns) promoted fp32
+// sums per row in registers.
 __host__ __device__ constexpr bool wide_slow(int bn, bool slow) { return slow && bn > 128; }
 // Tiles whose epilogue holds the whole tile in registers before storing it:
 // slow 256-column tiles (the promoted sums) and MX 256-column tiles, whose
@@ -148,7 +148,7 @@ struct KParams {
   unsigned* ws_counters;  // split-K arrivals per tile
   unsigned* amax_bits;    // fp32 amax as its bit pattern (non-negative floats order as uints)
   unsigned* abort_word;   // device word recording aborted waits (read by fp8mm_device_error)
-  uint32_t off_x, off_y, off_sf, off_out, off_ys, off_bar;  // shared-memory layout
+  uint32_t off_x, off_y, off_sf, off_out, off_ys, off_bias, off_bar;  // shared-memory layout
   uint32_t x_stage_bytes, y_stage_bytes, sf_stage_bytes;
   uint32_t out_swz_mask;  // 16-byte-chunk XOR mask of the output staging swizzle
   uint32_t out_rowbytes;  // bytes per staging row
@@ -273,20 +273,22 @@ __device__ __forceinline__ float bias_at(const KParams& p, int n) {
 // TMA copy at (cx, cy, cl).  xr is the thread's X row (the output column when
 // the operands are swapped).  v holds at least CW values (the chunk is its
 // first CW); NOSWAP drops the transposed staging of swapped operands.
+// With a bias, bias_cols points at the chunk's CW bias values staged in
+// shared memory (unswapped tiles; 0 past the last column) and bias_lane holds
+// the thread's own column's value (swapped tiles).
 template <int CW, int ES, int NV, bool NOSWAP = false>
 __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap* tm_c, float (&v)[NV], float alpha,
-                                            float sr, bool row_ok, int xr, int q0, int lane, uint8_t* stg_gen,
-                                            uint32_t stg_s, int cx, int cy, int cl, bool in_bounds, float& amax_f,
-                                            uint32_t& amax_nan) {
+                                            float sr, const float* bias_cols, float bias_lane, bool row_ok, int q0,
+                                            int lane, uint8_t* stg_gen, uint32_t stg_s, int cx, int cy, int cl,
+                                            bool in_bounds, float& amax_f, uint32_t& amax_nan) {
   if (ES != 1 && p.bias != nullptr) {
     // d = (a s_a) @ (b s_b)^T + bias: one fp32 fma, then the one rounding to out_dtype
     if (NOSWAP || !p.swap) {
 #pragma unroll
-      for (int i = 0; i < CW; ++i) v[i] = fmaf(v[i], alpha, (q0 + i < p.Q) ? bias_at(p, q0 + i) : 0.0f);
+      for (int i = 0; i < CW; ++i) v[i] = fmaf(v[i], alpha, bias_cols[i]);
     } else {
-      const float bv = row_ok ? bias_at(p, xr) : 0.0f;
 #pragma unroll
-      for (int i = 0; i < CW; ++i) v[i] = fmaf(v[i], alpha, bv);
+      for (int i = 0; i < CW; ++i) v[i] = fmaf(v[i], alpha, bias_lane);
     }
   } else {
 #pragma unroll
@@ -422,6 +424,7 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   const float alpha = p.sa_tensor ? (__ldg(p.sa_tensor) * __ldg(p.sb_tensor)) : 1.0f;
   const float sr = (ES == 1 && p.scale_result) ? __ldg(p.scale_result) : 1.0f;
   float* ys_w = reinterpret_cast<float*>(sgen + p.off_ys) + warp * HMAX;
+  float* bias_w = reinterpret_cast<float*>(sgen + p.off_bias) + warp * HMAX;  // this warp's columns' bias
   uint8_t* stg = sgen + p.off_out + warp * kStageOut;
   const uint32_t stg_s = sbase + p.off_out + warp * kStageOut;
   uint32_t stg_sel = 0;
@@ -697,6 +700,18 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
     // ---------------------------------------------------- scale, cast, store
     if (finish) {
       const int r0 = xbase + qd * 32;  // X row of the warp's first lane
+      // The bias of the warp's columns, staged once per tile (unswapped), or
+      // of the thread's own output column (swapped).
+      float bias_lane = 0.0f;
+      if (ES != 1 && p.bias != nullptr) {
+        if (!p.swap) {
+          const int qb = t.tq * BN + col0;
+          for (int j = lane; j < ncols; j += 32) bias_w[j] = (qb + j < p.Q) ? bias_at(p, qb + j) : 0.0f;
+          __syncwarp();
+        } else if (row_ok) {
+          bias_lane = bias_at(p, xr);
+        }
+      }
       auto finish_chunk = [&](int ci) {
         if constexpr (HOLD) {
           // The held sums are stored in place: the chunk is acc[0 .. CW),
@@ -705,7 +720,8 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
           float v[CW];
 #pragma unroll
           for (int i = 0; i < CW; ++i) v[i] = acc(i);
-          store_chunk<CW, ES, CW, true>(p, tm_c, v, alpha, sr, row_ok, xr, q0, lane, stg + stg_sel * (kStageOut / 2),
+          store_chunk<CW, ES, CW, true>(p, tm_c, v, alpha, sr, bias_w + ci * CW, bias_lane, row_ok, q0, lane,
+                                          stg + stg_sel * (kStageOut / 2),
                                           stg_s + stg_sel * (kStageOut / 2), q0, r0, t.l, q0 < p.Q && r0 < p.R,
                                           amax_f, amax_nan);
           stg_sel ^= 1u;
@@ -740,7 +756,8 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
             for (int i = 0; i < CW; ++i) v[i] = sum[i];
           }
           const int q0 = t.tq * BN + col0 + ci * CW;  // Y row of the chunk's first column
-          store_chunk<CW, ES>(p, tm_c, v, alpha, sr, row_ok, xr, q0, lane, stg + stg_sel * (kStageOut / 2),
+          store_chunk<CW, ES>(p, tm_c, v, alpha, sr, bias_w + ci * CW, bias_lane, row_ok, q0, lane,
+                              stg + stg_sel * (kStageOut / 2),
                               stg_s + stg_sel * (kStageOut / 2), p.swap ? r0 : q0, p.swap ? q0 : r0, t.l,
                               q0 < p.Q && r0 < p.R, amax_f, amax_nan);
           stg_sel ^= 1u;
@@ -766,12 +783,14 @@ template <int BN, bool SLOW, bool MX, int CG, int EW, bool F4 = false>
 __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1)
     fp8mm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                  const __grid_constant__ CUtensorMap tm_c, const KParams p) {
-  static_assert(!F4 || (MX && BN == 128 && !SLOW && CG == 1), "FP4: 128-column block-scaled tiles, fast");
+  static_assert(!F4 || (MX && (BN == 128 || BN == 256) && !SLOW && CG == 1),
+                "FP4: 128- or 256-column block-scaled tiles, fast");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(!MX || BN == 128 || BN == 256 || (BN % 32 == 0 && BN < 256),
                 "MX tiles start on a 32-row boundary of a factor atom");
-  static_assert(!SLOW || BN <= 128 || ((BN == 256 || BN == 224) && !MX && EW == 8) || (BN == 256 && CG == 1 && !MX),
-                "slow accumulation keeps its promoted sums in registers: 224- or 256-column tiles");
+  static_assert(!SLOW || BN <= 128 || ((BN == 256 || BN == 224 || BN == 192) && !MX && EW == 8) ||
+                    (BN == 256 && CG == 1 && !MX),
+                "slow accumulation keeps its promoted sums in registers: 192-, 224- or 256-column tiles");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
   static_assert(!MX || CG == 1, "the block-scaled form runs on single-CTA tiles");
   extern __shared__ uint8_t smem_raw[];
@@ -790,8 +809,8 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
   if constexpr (held_tile(BN, SLOW, MX)) {
-    // Held tiles are planned without split-K or swapped operands, and a
-    // 224-column tile (whose halves straddle 128-column blocks) without
+    // Held tiles are planned without split-K or swapped operands, and 192-
+    // or 224-column tiles (whose halves straddle 128-column blocks) without
     // 128x128 Y scales.
     if (p.splits != 1 || p.swap || (BN % 128 != 0 && p.y_kind == kScaleBlock128)) {
       if (threadIdx.x == 0) atomicOr(p.abort_word, kErrPlan);
@@ -881,7 +900,7 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           // FP4: the atoms that exist for this stage's 256 elements of K
           const int f4_na = F4 ? min(apk, p.scale_kb - kb * apk) : 0;
-          const uint32_t tx = tx0 + (F4 ? 1024u * (uint32_t)f4_na : 0u);
+          const uint32_t tx = tx0 + (F4 ? 512u * (uint32_t)f4_na * (1 + BN / 128) : 0u);
           {
             bool w = wait_bar(bar_empty + 8u * stage, phase ^ 1u, abort_flag, p.abort_word, kErrProducer);
             if constexpr (GATHER) w = __all_sync(0xFFFFFFFFu, w);  // the lanes leave together
@@ -905,13 +924,19 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
             ptx::tma_load_3d(sbase + p.off_y + stage * p.y_stage_bytes, &tm_y, fb, kb * kBlockK, yrow0, t.l);
           }
           if constexpr (F4) {
-            // X atoms in slots 0 .. apk-1, Y atoms in slots apk .. 2 apk-1
+            // X atoms in slots 0 .. apk-1, then the atoms of each 128-row block
+            // of the Y tile (apk slots each).  A row block's atoms lie
+            // contiguous along K: one copy per operand and row block.  Blocks
+            // past the last one are clamped to it; their rows are never stored.
             const uint32_t sf = sbase + p.off_sf + stage * p.sf_stage_bytes;
-            for (int i = 0; i < f4_na; ++i) {
-              const size_t a = (size_t)kb * apk + i;
-              ptx::bulk_load(sf + 512u * i, p.sfx + (((size_t)t.l * p.sfx_mb + t.tr) * p.scale_kb + a) * 512u, 512u, fb);
-              ptx::bulk_load(sf + 512u * (apk + i), p.sfy + (((size_t)t.l * p.sfy_mb + t.tq) * p.scale_kb + a) * 512u,
-                             512u, fb);
+            const size_t a0 = (size_t)kb * apk;
+            ptx::bulk_load(sf, p.sfx + (((size_t)t.l * p.sfx_mb + t.tr) * p.scale_kb + a0) * 512u,
+                           512u * (uint32_t)f4_na, fb);
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j) {
+              const int mb = min(t.tq * (BN / 128) + j, p.sfy_mb - 1);
+              ptx::bulk_load(sf + 512u * apk * (1 + j), p.sfy + (((size_t)t.l * p.sfy_mb + mb) * p.scale_kb + a0) * 512u,
+                             512u * (uint32_t)f4_na, fb);
             }
           } else if constexpr (MX) {
             const uint32_t sf = sbase + p.off_sf + stage * p.sf_stage_bytes;
@@ -990,15 +1015,22 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
           const uint64_t adesc = ptx::desc_sw128_kmajor(sbase + p.off_x + stage * p.x_stage_bytes);
           const uint64_t bdesc = ptx::desc_sw128_kmajor(sbase + p.off_y + stage * p.y_stage_bytes);
           if constexpr (F4) {
-            // TMEM slot of 8 apk columns per stage: X's atoms, then Y's, 4 columns each.
+            // TMEM slot of 4 apk (1 + BN/128) columns per stage: X's atoms (4
+            // columns each), then for each K atom the Y tile's row blocks side
+            // by side, so that one MMA reads its BN rows' factors from adjacent
+            // columns (row r of the tile in column r / 32).
+            constexpr int NYB = BN / 128;
             const int apk = p.f4_vec16 ? 4 : 2;
             const int na = min(apk, p.scale_kb - kb * apk);
             const uint32_t sf_smem = sbase + p.off_sf + stage * p.sf_stage_bytes;
-            const uint32_t sf_x = tmem_base + (uint32_t)(p.num_acc * BN) + stage * (uint32_t)(8 * apk);
+            const uint32_t sf_x = tmem_base + (uint32_t)(p.num_acc * BN) + stage * (uint32_t)(4 * apk * (1 + NYB));
             const uint32_t sf_y = sf_x + 4u * (uint32_t)apk;
             for (int i = 0; i < na; ++i) {
               ptx::tmem_cp_32x128b_warpx4(sf_x + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * i));
-              ptx::tmem_cp_32x128b_warpx4(sf_y + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * (apk + i)));
+#pragma unroll
+              for (int j = 0; j < NYB; ++j)
+                ptx::tmem_cp_32x128b_warpx4(sf_y + 4u * (uint32_t)(NYB * i + j),
+                                            ptx::desc_sf_atom(sf_smem + 512u * (uint32_t)(apk * (1 + j) + i)));
             }
 #pragma unroll
             for (int k = 0; k < kBlockK / 32; ++k) {
@@ -1006,12 +1038,13 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
               if (kb * 256 + 64 * k >= p.K) break;
               const uint32_t acc = (!gstart || k > 0) ? 1u : 0u;
               if (p.f4_vec16) {
-                ptx::mma_mxf4nvf4_4x(d, adesc + 2u * k, bdesc + 2u * k, p.idesc, sf_x + 4u * k, sf_y + 4u * k, acc);
+                ptx::mma_mxf4nvf4_4x(d, adesc + 2u * k, bdesc + 2u * k, p.idesc, sf_x + 4u * k,
+                                     sf_y + 4u * (uint32_t)(NYB * k), acc);
               } else {
                 // the atom holds 4 factors per row: MMA k reads bytes 2 (k % 2) .. +1 of atom k / 2
                 const uint32_t id = (uint32_t)(k & 1) * 2u;
                 ptx::mma_mxf4nvf4_2x(d, adesc + 2u * k, bdesc + 2u * k, p.idesc | (id << 29) | (id << 4),
-                                     sf_x + 4u * (k >> 1), sf_y + 4u * (k >> 1), acc);
+                                     sf_x + 4u * (k >> 1), sf_y + 4u * (uint32_t)(NYB * (k >> 1)), acc);
               }
             }
           } else if constexpr (MX) {

@@ -33,12 +33,15 @@ KernelFn kernel_bn128_slow_f8_cg1_ew16();
 KernelFn kernel_bn256_slow_f8_cg1_ew8();
 KernelFn kernel_bn256_slow_f8_cg1_ew16();
 KernelFn kernel_bn256_slow_f8_cg2_ew8();
+KernelFn kernel_bn224_slow_f8_cg1_ew8();
+KernelFn kernel_bn192_slow_f8_cg1_ew8();
 KernelFn kernel_bn224_slow_f8_cg2_ew8();
 KernelFn kernel_bn128_fast_mx_cg1_ew8();
 KernelFn kernel_bn224_fast_mx_cg1_ew8();
 KernelFn kernel_bn256_fast_mx_cg1_ew8();
 KernelFn kernel_bn128_slow_mx_cg1_ew8();
 KernelFn kernel_bn128_fast_f4_cg1_ew8();
+KernelFn kernel_bn256_fast_f4_cg1_ew8();
 
 struct KernelEntry {
   int bn, slow, mx, cg, ew, f4;
@@ -66,12 +69,15 @@ inline const KernelEntry* kernel_table(int* n) {
       {256, 1, 0, 1, 8, 0, &kernel_bn256_slow_f8_cg1_ew8},
       {256, 1, 0, 1, 16, 0, &kernel_bn256_slow_f8_cg1_ew16},
       {256, 1, 0, 2, 8, 0, &kernel_bn256_slow_f8_cg2_ew8},
+      {224, 1, 0, 1, 8, 0, &kernel_bn224_slow_f8_cg1_ew8},
+      {192, 1, 0, 1, 8, 0, &kernel_bn192_slow_f8_cg1_ew8},
       {224, 1, 0, 2, 8, 0, &kernel_bn224_slow_f8_cg2_ew8},
       {128, 0, 1, 1, 8, 0, &kernel_bn128_fast_mx_cg1_ew8},
       {224, 0, 1, 1, 8, 0, &kernel_bn224_fast_mx_cg1_ew8},
       {256, 0, 1, 1, 8, 0, &kernel_bn256_fast_mx_cg1_ew8},
       {128, 1, 1, 1, 8, 0, &kernel_bn128_slow_mx_cg1_ew8},
       {128, 0, 1, 1, 8, 1, &kernel_bn128_fast_f4_cg1_ew8},
+      {256, 0, 1, 1, 8, 1, &kernel_bn256_fast_f4_cg1_ew8},
   };
   *n = (int)(sizeof(table) / sizeof(table[0]));
   return table;

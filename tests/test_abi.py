@@ -82,7 +82,7 @@ int main(void) {
     subprocess.run(["gcc", "-I" + os.path.join(ROOT, "include"), str(src), "-L" + libdir, "-lfp8mm",
                     "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
-    assert out[0].split()[1:] == ["256", "0", "1", "1"]
+    assert out[0].split()[1:] == ["224", "0", "1", "1"]  # one-CTA held 128 x 224 tiles: four whole waves
     assert "ALIGN" in out[1].upper()
 
 
@@ -108,7 +108,7 @@ def _plan_status(**kw):
     (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=0), B.FP8MM_ERR_UNSUPPORTED),  # FP4 needs factors
     (dict(M=16, N=16, K=32, a_fmt=2, b_fmt=2, scale_mode=4), B.FP8MM_ERR_ALIGNMENT),    # K % 64
     (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=4, fast_accum=0), B.FP8MM_ERR_UNSUPPORTED),
-    (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=4, block_n=256), B.FP8MM_ERR_UNSUPPORTED),
+    (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=4, block_n=224), B.FP8MM_ERR_UNSUPPORTED),
     (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=4), B.FP8MM_OK),
     (dict(M=16, N=16, K=64, a_fmt=2, b_fmt=2, scale_mode=3), B.FP8MM_OK),
     (dict(M=16, N=16, K=16, out_dtype=5), B.FP8MM_ERR_INVALID),

@@ -55,3 +55,13 @@ def test_fp4_batched_4x4096(form):
     p = synth.fp4_batched(form=form, seed=98 if form == "nv16" else 99)
     rows = sorted({0, 1, 127, 128, 2047, 4095} | {int(x) for x in np.linspace(0, 4095, 6)})
     _run_check(p, rows=rows)
+
+
+@pytest.mark.parametrize("form", ["nv16", "mx32"])
+@pytest.mark.parametrize("out", [synth.OUT_F32, synth.OUT_BF16])
+def test_fp4_wide_tiles(form, out):
+    # 256-column held tiles: X's factor atoms and both 128-row blocks of Y's per
+    # stage; the last tile's second row block lies past N and is clamped
+    p = synth.fp4_batched(L=2, M=264, N=520, K=576, form=form, seed=100, out_dtype=out)
+    c, amax, plan = _run_check(p, block_n=256)
+    assert plan.info()["block_n"] == 256

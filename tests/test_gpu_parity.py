@@ -326,3 +326,18 @@ def test_slow_pair_held_batched_multiwave():
     p = synth.llm_per_tensor(L=2, M=1280, N=2240, K=512, seed=49, fast_accum=False)
     c, amax, plan = _run_check(p, block_n=224, cta_pair=1)
     assert plan.info()["units"] > 76
+
+
+@pytest.mark.parametrize("block_n", [192, 224])
+@pytest.mark.parametrize("case", ["tensor_bf16", "tensor_f32", "block1"])
+def test_slow_held_one_cta_192_224(case, block_n):
+    # one-CTA held slow tiles of 192 / 224 columns (96 / 112 promoted sums per
+    # epilogue thread); ragged in M, N and K
+    if case.startswith("tensor"):
+        out = synth.OUT_BF16 if case.endswith("bf16") else synth.OUT_F32
+        p = synth.llm_per_tensor(M=300, N=520, K=640, seed=50, fast_accum=False, out_dtype=out)
+    else:
+        p = synth.blockwise(M=300, N=520, K=640, seed=51, b_block=1)
+    c, amax, plan = _run_check(p, block_n=block_n, cta_pair=2, swap_ab=2)
+    info = plan.info()
+    assert (info["block_n"], info["cta_pair"], info["splitk"]) == (block_n, 0, 1)

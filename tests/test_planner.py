@@ -37,10 +37,11 @@ def test_llm_4096_fast_uses_pair_tiles(lib):
     assert i["units"] == 16 * 19 and i["stages"] == 6 and i["grid"] == SMS
 
 
-def test_llm_4096_slow_uses_held_256_column_tiles(lib):
+def test_llm_4096_slow_uses_held_224_column_tiles(lib):
+    # one-CTA held tiles: 32 x 19 = 608 tiles of 128 x 224, exactly four waves over 152 SMs
     i = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0)
-    assert (i["cta_pair"], i["block_n"], i["splitk"], i["epi_warps"], i["slow"]) == (0, 256, 1, 8, 1)
-    assert i["stages"] == 4
+    assert (i["cta_pair"], i["block_n"], i["splitk"], i["epi_warps"], i["slow"]) == (0, 224, 1, 8, 1)
+    assert i["stages"] == 4 and i["units"] == 32 * 19
     # held slow tiles on CTA pairs only on request (measured slower)
     j = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0, cta_pair=1, block_n=224)
     assert (j["cta_pair"], j["block_n"], j["stages"], j["units"]) == (1, 224, 6, 16 * 19)
@@ -60,7 +61,7 @@ def test_mx_batched_held_256(lib):
 
 @pytest.mark.parametrize("M,fast,swap,bn,splitk,pair", [
     (16, 1, 1, 16, 2, 0), (16, 0, 1, 16, 2, 0), (64, 1, 1, 64, 2, 0),
-    (256, 1, 0, 224, 1, 1), (256, 0, 0, 256, 1, 0), (1024, 0, 0, 256, 1, 0), (2048, 0, 0, 256, 1, 0),
+    (256, 1, 0, 224, 1, 1), (256, 0, 0, 192, 1, 0), (1024, 0, 0, 256, 1, 0), (2048, 0, 0, 256, 1, 0),
     (1024, 1, 0, 256, 1, 1), (2048, 1, 0, 256, 1, 1), (8192, 1, 0, 256, 1, 1), (8192, 0, 0, 256, 1, 0),
 ])
 def test_skinny_sweep(lib, M, fast, swap, bn, splitk, pair):
@@ -80,7 +81,8 @@ def test_workspace_free_plans_have_no_split(lib):
     (dict(cta_pair=1, scale_mode=B.FP8MM_SCALE_MX32_UE8M0), B.FP8MM_ERR_UNSUPPORTED),
     (dict(block_n=256, fast_accum=0, epi_warps=16), B.FP8MM_OK),
     (dict(block_n=224, fast_accum=0, cta_pair=1), B.FP8MM_OK),                       # held slow pair tile
-    (dict(block_n=224, fast_accum=0, cta_pair=2), B.FP8MM_ERR_UNSUPPORTED),         # 224 held only on pairs
+    (dict(block_n=224, fast_accum=0, cta_pair=2), B.FP8MM_OK),                      # 224 held on one CTA
+    (dict(block_n=192, fast_accum=0, cta_pair=1), B.FP8MM_ERR_UNSUPPORTED),         # 192 held on one CTA only
     (dict(block_n=224, cta_pair=1, scale_mode=B.FP8MM_SCALE_A1x128_B128x128), B.FP8MM_ERR_UNSUPPORTED),
     (dict(block_n=224, cta_pair=1, scale_mode=B.FP8MM_SCALE_A1x128_B1x128), B.FP8MM_OK),
     (dict(block_n=256, fast_accum=0, cta_pair=1, epi_warps=16), B.FP8MM_ERR_UNSUPPORTED),
