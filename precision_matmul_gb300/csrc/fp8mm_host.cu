@@ -288,8 +288,13 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // Y bytes per MMA, which measured 4-15% faster than single-CTA tiles on
   // GB300 for fast unswapped GEMMs with at least one wave of pairs.
   const int64_t pair_rows = std::max<int64_t>(1, cdiv(P->R, 2 * kBlockM));
+  // MX (FP8 operands) pairs: 256-column tiles only, each CTA staging its own
+  // rows' factor atom and all of the Y tile's.  Planned only on request: on
+  // GB300 they measured no faster than one-CTA held tiles (4 x 4096^3: 246 vs
+  // 237 us), whose time per stage they share.
+  const bool mx_pairable = mx && !f4 && !P->slow;
   const bool auto_pair = d.cta_pair == 0 && !mx && !P->slow && !swap && P->Q > 128 &&
-                         (d.block_n == 0 || d.block_n == 224 || d.block_n == 256) &&
+                         (d.block_n == 0 || (d.block_n == 224 && !mx) || d.block_n == 256) &&
                          pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
   // Slow accumulation on CTA pairs (256-row held tiles of 224 or 256 columns)
   // is built but only planned on request (cta_pair = 1): each 128-K chunk is
@@ -304,6 +309,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
     // the width whose whole waves over the SM pairs cost least
     double best = 1e300;
     for (int c : {256, 224}) {
+      if (mx && c != 256) continue;
       const int64_t tiles = pair_rows * cdiv(P->Q, c) * L;
       const double cost = (double)cdiv(tiles, P->sms / 2) * c / width_efficiency(c, false);
       if (cost < best * 0.999) {
@@ -381,7 +387,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   P->bn = bn;
 
   if (d.cta_pair == 1 || auto_pair) {
-    if (mx || swap) return FP8MM_ERR_UNSUPPORTED;
+    if ((mx && !(mx_pairable && bn == 256)) || swap) return FP8MM_ERR_UNSUPPORTED;
     P->cg = 2;
   }
   // Epilogue warps: 16 for slow accumulation at 128 columns (more TMEM loads
@@ -696,7 +702,9 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
   if (!enc) return FP8MM_ERR_CUDA;
   const void* xptr = P->swap ? b : a;
   const void* yptr = P->swap ? a : b;
-  CUtensorMap tm_x, tm_y, tm_c;
+  CUtensorMap tm_x, tm_y, tm_c, tm_sfx, tm_sfy;
+  std::memset(&tm_sfx, 0, sizeof(tm_sfx));
+  std::memset(&tm_sfy, 0, sizeof(tm_sfy));
   const int64_t kbytes = P->f4 ? d.K / 2 : d.K;  // bytes of K per operand row (FP4: two elements per byte)
   {
     cuuint64_t dims[3] = {(cuuint64_t)kbytes, (cuuint64_t)P->R, (cuuint64_t)d.L};
@@ -833,7 +841,28 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
   KernelFn fn = select_kernel(P->bn, P->slow != 0, P->mx != 0, P->cg, P->ew, P->f4 != 0);
   if (!fn) return FP8MM_ERR_UNSUPPORTED;
   if (ensure_smem_attr(fn, d.device, (size_t)P->max_smem) != cudaSuccess) return FP8MM_ERR_CUDA;
-  void* args[4] = {&tm_x, &tm_y, &tm_c, &kp};
+  if (P->mx && !P->f4 && P->cg == 2) {
+    // The factor atoms as a [atoms][2][256] byte tensor: one 512-byte box per
+    // atom, loaded by the pair form of the TMA so that both CTAs' copies
+    // complete on the leader's barrier.
+    const void* sfx_ptr = P->swap ? scale_b : scale_a;
+    const void* sfy_ptr = P->swap ? scale_a : scale_b;
+    const int64_t kbn = P->num_kb;
+    const int64_t natoms[2] = {(int64_t)d.L * cdiv(P->R, 128) * kbn, (int64_t)d.L * cdiv(P->Q, 128) * kbn};
+    const void* ptrs[2] = {sfx_ptr, sfy_ptr};
+    CUtensorMap* maps[2] = {&tm_sfx, &tm_sfy};
+    for (int i = 0; i < 2; ++i) {
+      cuuint64_t dims[3] = {256, 2, (cuuint64_t)natoms[i]};
+      cuuint64_t strides[2] = {256, 512};
+      cuuint32_t box[3] = {256, 2, 1};
+      cuuint32_t es[3] = {1, 1, 1};
+      if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptrs[i]), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return FP8MM_ERR_CUDA;
+    }
+  }
+  void* args[6] = {&tm_x, &tm_y, &tm_c, &tm_sfx, &tm_sfy, &kp};
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -782,7 +782,8 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
 template <int BN, bool SLOW, bool MX, int CG, int EW, bool F4 = false>
 __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1)
     fp8mm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
-                 const __grid_constant__ CUtensorMap tm_c, const KParams p) {
+                 const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_sfx,
+                 const __grid_constant__ CUtensorMap tm_sfy, const KParams p) {
   static_assert(!F4 || (MX && (BN == 128 || BN == 256) && !SLOW && CG == 1),
                 "FP4: 128- or 256-column block-scaled tiles, fast");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
@@ -792,7 +793,7 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
                     (BN == 256 && CG == 1 && !MX),
                 "slow accumulation keeps its promoted sums in registers: 192-, 224- or 256-column tiles");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
-  static_assert(!MX || CG == 1, "the block-scaled form runs on single-CTA tiles");
+  static_assert(!MX || CG == 1 || (BN == 256 && !SLOW && !F4), "block-scaled CTA pairs: fast FP8 256-column tiles");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sraw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (sraw + 1023u) & ~1023u;
@@ -895,7 +896,7 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
         // MX: Y's tile may start inside a 128-row atom; copy every atom it touches.
         const int y_atom0 = (t.tq * BN) / 128;
         const int y_atoms = (MX && !GATHER) ? ((t.tq * BN) % 128 + BN + 127) / 128 : 0;
-        const uint32_t tx0 = CG * (p.x_stage_bytes + p.y_stage_bytes) + ((MX && !F4) ? 512u * (1 + y_atoms) : 0u);
+        const uint32_t tx0 = CG * (p.x_stage_bytes + p.y_stage_bytes + ((MX && !F4) ? 512u * (1 + y_atoms) : 0u));
         const int apk = p.f4_vec16 ? 4 : 2;  // FP4: factor atoms per stage and operand
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           // FP4: the atoms that exist for this stage's 256 elements of K
@@ -937,6 +938,22 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
               const int mb = min(t.tq * (BN / 128) + j, p.sfy_mb - 1);
               ptx::bulk_load(sf + 512u * apk * (1 + j), p.sfy + (((size_t)t.l * p.sfy_mb + mb) * p.scale_kb + a0) * 512u,
                              512u * (uint32_t)f4_na, fb);
+            }
+          } else if constexpr (MX && CG == 2) {
+            // CTA pair: each CTA stages the factor atom of its own 128 rows of
+            // X and every atom of the Y tile (the pair MMA reads all of Y's
+            // factors from each CTA's TMEM).  The copies go through TMA
+            // tensor maps over the atoms, so that they complete on the
+            // leader's full barrier like the operand tiles.
+            const uint32_t sf = sbase + p.off_sf + stage * p.sf_stage_bytes;
+            const uint32_t fb_leader = ptx::mapa_shared(fb, 0u);
+            const int xmb = min(t.tr * 2 + (int)rank, p.sfx_mb - 1);
+            ptx::tma_load_3d_pair(sf, &tm_sfx, fb_leader, 0, 0,
+                                  (int)(((size_t)t.l * p.sfx_mb + xmb) * p.scale_kb + kb));
+            for (int i = 0; i < y_atoms; ++i) {
+              const int mb = min(y_atom0 + i, p.sfy_mb - 1);
+              ptx::tma_load_3d_pair(sf + 512u * (1 + i), &tm_sfy, fb_leader, 0, 0,
+                                    (int)(((size_t)t.l * p.sfy_mb + mb) * p.scale_kb + kb));
             }
           } else if constexpr (MX) {
             const uint32_t sf = sbase + p.off_sf + stage * p.sf_stage_bytes;
@@ -1057,15 +1074,26 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
             // (224-column tiles) start at the tile's first row: column 4.
             const int y_atoms = GATHER ? (BN + 127) / 128 : ((t.tq * BN) % 128 + BN + 127) / 128;
             const uint32_t sf_y = sf_x + 4u + (GATHER ? 0u : (uint32_t)(((t.tq * BN) % 128) / 32));
-            ptx::tmem_cp_32x128b_warpx4(sf_x, ptx::desc_sf_atom(sf_smem));
-            for (int i = 0; i < y_atoms; ++i)
-              ptx::tmem_cp_32x128b_warpx4(sf_x + 4u + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * (1 + i)));
+            if constexpr (CG == 2) {
+              // each CTA copies its own staged atoms into its own TMEM
+              ptx::tmem_cp_32x128b_warpx4_pair(sf_x, ptx::desc_sf_atom(sf_smem));
+              for (int i = 0; i < y_atoms; ++i)
+                ptx::tmem_cp_32x128b_warpx4_pair(sf_x + 4u + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * (1 + i)));
+            } else {
+              ptx::tmem_cp_32x128b_warpx4(sf_x, ptx::desc_sf_atom(sf_smem));
+              for (int i = 0; i < y_atoms; ++i)
+                ptx::tmem_cp_32x128b_warpx4(sf_x + 4u + 4u * i, ptx::desc_sf_atom(sf_smem + 512u * (1 + i)));
+            }
 #pragma unroll
             for (int k = 0; k < kBlockK / kUmmaK; ++k) {
               // scale-factor ids pick byte k of each 32-bit TMEM word: the K block of 32
               const uint32_t idesc = p.idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4);
-              ptx::mma_mxf8f6f4(d, adesc + 2u * k, bdesc + 2u * k, idesc, sf_x, sf_y,
-                                (!gstart || k > 0) ? 1u : 0u);
+              if constexpr (CG == 2)
+                ptx::mma_mxf8f6f4_pair(d, adesc + 2u * k, bdesc + 2u * k, idesc, sf_x, sf_y,
+                                       (!gstart || k > 0) ? 1u : 0u);
+              else
+                ptx::mma_mxf8f6f4(d, adesc + 2u * k, bdesc + 2u * k, idesc, sf_x, sf_y,
+                                  (!gstart || k > 0) ? 1u : 0u);
             }
           } else if constexpr (CG == 2) {
 #pragma unroll
@@ -1144,5 +1172,6 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
 }  // namespace fp8mm
 
 namespace fp8mm {
-using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const KParams);
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                          const KParams);
 }  // namespace fp8mm

@@ -39,6 +39,7 @@ KernelFn kernel_bn224_slow_f8_cg2_ew8();
 KernelFn kernel_bn128_fast_mx_cg1_ew8();
 KernelFn kernel_bn224_fast_mx_cg1_ew8();
 KernelFn kernel_bn256_fast_mx_cg1_ew8();
+KernelFn kernel_bn256_fast_mx_cg2_ew8();
 KernelFn kernel_bn128_slow_mx_cg1_ew8();
 KernelFn kernel_bn128_fast_f4_cg1_ew8();
 KernelFn kernel_bn256_fast_f4_cg1_ew8();
@@ -75,6 +76,7 @@ inline const KernelEntry* kernel_table(int* n) {
       {128, 0, 1, 1, 8, 0, &kernel_bn128_fast_mx_cg1_ew8},
       {224, 0, 1, 1, 8, 0, &kernel_bn224_fast_mx_cg1_ew8},
       {256, 0, 1, 1, 8, 0, &kernel_bn256_fast_mx_cg1_ew8},
+      {256, 0, 1, 2, 8, 0, &kernel_bn256_fast_mx_cg2_ew8},
       {128, 1, 1, 1, 8, 0, &kernel_bn128_slow_mx_cg1_ew8},
       {128, 0, 1, 1, 8, 1, &kernel_bn128_fast_f4_cg1_ew8},
       {256, 0, 1, 1, 8, 1, &kernel_bn256_fast_f4_cg1_ew8},

@@ -274,6 +274,25 @@ __device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled two-SM MMA (one UE8M0 factor per row per 32 elements of K):
+// each CTA's TMEM holds the factors of its own 128 rows of A at sfa_tmem and
+// the factors of all N rows of B at sfb_tmem.
+__device__ __forceinline__ void mma_mxf8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Issued by the pair leader: each CTA copies the 32 x 128-bit matrix at
+// `sdesc` in its own shared memory into its own TMEM (lanes 0-31, replicated
+// into the other quarters).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 // Arrive once on the mbarrier at the same offset in every CTA of `mask` when the
 // pair's tcgen05 operations issued so far complete.
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {

@@ -341,3 +341,26 @@ def test_slow_held_one_cta_192_224(case, block_n):
     c, amax, plan = _run_check(p, block_n=block_n, cta_pair=2, swap_ab=2)
     info = plan.info()
     assert (info["block_n"], info["cta_pair"], info["splitk"]) == (block_n, 0, 1)
+
+
+@pytest.mark.parametrize("fmt", [synth.E4M3, synth.E5M2])
+@pytest.mark.parametrize("out", [synth.OUT_F32, synth.OUT_BF16])
+def test_mx_pair_tiles(fmt, out):
+    # block-scaled MMAs on CTA pairs: 256 x 256 held tiles; each CTA stages its own
+    # rows' factor atom and both of the Y tile's; ragged in M (a half-empty second
+    # CTA), N (a last tile past N) and K, over a batch of two
+    p = synth.mx_batched(L=2, M=392, N=600, K=416, fmt=fmt, seed=52, out_dtype=out)
+    c, amax, plan = _run_check(p, block_n=256, cta_pair=1)
+    info = plan.info()
+    assert (info["block_n"], info["cta_pair"]) == (256, 1)
+
+
+def test_mx_pair_tiles_multiwave_with_fp8_output():
+    p = synth.mx_batched(L=3, M=1024, N=2304, K=512, seed=53, out_dtype=synth.OUT_E4M3)
+    p.scale_a.fill_(127 - 8)
+    p.scale_b.fill_(127 - 8)
+    c, amax, plan = run_gpu(p, block_n=256, cta_pair=1, scale_result=1.0)
+    torch.cuda.synchronize()
+    assert pm.fp8mm_device_error(0) == 0
+    check(p, c, amax, scale_result=1.0)
+    assert plan.info()["cta_pair"] == 1 and plan.info()["units"] > 76

@@ -57,6 +57,9 @@ def test_mx_batched_held_256(lib):
     i = preview(4096, 4096, 4096, 4, scale_mode=B.FP8MM_SCALE_MX32_UE8M0, out_dtype=0, fast_accum=1)
     assert (i["block_n"], i["cta_pair"], i["splitk"], i["stages"]) == (256, 0, 1, 4)
     assert i["units"] == 4 * 32 * 16
+    # on request: 256 x 256 held tiles on CTA pairs, 6 stages of 34 KiB per SM
+    j = preview(4096, 4096, 4096, 4, scale_mode=B.FP8MM_SCALE_MX32_UE8M0, out_dtype=0, fast_accum=1, cta_pair=1)
+    assert (j["block_n"], j["cta_pair"], j["stages"], j["units"]) == (256, 1, 6, 4 * 16 * 16)
 
 
 @pytest.mark.parametrize("M,fast,swap,bn,splitk,pair", [
@@ -78,7 +81,9 @@ def test_workspace_free_plans_have_no_split(lib):
     (dict(block_n=256, fast_accum=0, splitk=2), B.FP8MM_ERR_UNSUPPORTED),           # held tiles are never split
     (dict(block_n=192, scale_mode=B.FP8MM_SCALE_MX32_UE8M0), B.FP8MM_ERR_UNSUPPORTED),  # MX widths 128/224/256
     (dict(block_n=224, scale_mode=B.FP8MM_SCALE_MX32_UE8M0), B.FP8MM_OK),
-    (dict(cta_pair=1, scale_mode=B.FP8MM_SCALE_MX32_UE8M0), B.FP8MM_ERR_UNSUPPORTED),
+    (dict(cta_pair=1, scale_mode=B.FP8MM_SCALE_MX32_UE8M0, block_n=128), B.FP8MM_ERR_UNSUPPORTED),  # MX pairs: 256
+    (dict(cta_pair=1, scale_mode=B.FP8MM_SCALE_MX32_UE8M0, block_n=256), B.FP8MM_OK),
+    (dict(cta_pair=1, scale_mode=B.FP8MM_SCALE_MX32_UE8M0, block_n=256, fast_accum=0), B.FP8MM_ERR_UNSUPPORTED),
     (dict(block_n=256, fast_accum=0, epi_warps=16), B.FP8MM_OK),
     (dict(block_n=224, fast_accum=0, cta_pair=1), B.FP8MM_OK),                       # held slow pair tile
     (dict(block_n=224, fast_accum=0, cta_pair=2), B.FP8MM_OK),                      # 224 held on one CTA
