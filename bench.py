@@ -41,7 +41,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "FP8 scaled-GEMM TFLOP/s (+GB/s) at 1 GB300 and % of FP8/HBM roofline"
-KERNEL_SOURCES = ["precision_matmul_gb300/csrc/fp8mm_kernel.cuh", "precision_matmul_gb300/csrc/ptx.cuh"]
+# the kernels and the planner (tile shapes and raster decide the DRAM traffic a capture records)
+KERNEL_SOURCES = ["precision_matmul_gb300/csrc/fp8mm_kernel.cuh", "precision_matmul_gb300/csrc/ptx.cuh",
+                  "precision_matmul_gb300/csrc/fp8mm_host.cu", "precision_matmul_gb300/csrc/fp8mm_aux.cu"]
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 FP8_NOMINAL_TFLOPS = 4500.0
 FP4_PER_BF16 = 6.0  # nominal dense FP4 : BF16 tensor rate on GB300 (13.5 : 2.25 PFLOP/s)
