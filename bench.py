@@ -18,7 +18,8 @@ the copy bandwidth); ``roofline`` is the dominant call of the step.
 configurations: an FP8 output, a bias, the NN layout, NVFP4 / MXFP4 operands
 and a batched GEMM with b given K-outermost.  ``e2e``
 is the same metric through the public API with each call's operands copied
-from pinned host memory and C and amax read back, inside the timed region.
+from pinned host memory and C and amax read back, inside the timed region
+(copies on their own streams, overlapping the GEMMs as a user's pipeline would).
 ``--impl reference`` times the CPU oracle instead (a bounded sample of every
 call on the host cores).  Subsets with ``--workload`` (comma-separated names
 or groups: c1 .. c5, mx, skinny, or a single call name).
@@ -508,31 +509,63 @@ def run_ours(args, rank, world, local_rank):
                      "tflops": probs[sus_idx][2].flops * n_calls / s_s / 1e12, "clocks": sclk.summary(),
                      "note": "back to back, no L2 flush (the operands stay in L2)"}
 
-    # ---- e2e through the public API: pinned host operands in, C and amax out
-    host = []
+    # ---- e2e through the public API: pinned host operands in, C and amax out.
+    # As a user of the library would pipeline it: each call's operands are
+    # copied in on a copy stream (one call ahead of the compute), the GEMM runs
+    # on the current stream, and C and amax are read back on a third stream.
+    # Every call has its own device operands, so no copy overwrites operands a
+    # GEMM may still read; a call's C is rewritten only after its previous
+    # read-back has finished.
+    host, dev_in = [], []
     for p, a, b, sa, sb, c, amax, _ in ins:
         host.append((a.cpu().pin_memory(), b.cpu().pin_memory(), sa.cpu().pin_memory(), sb.cpu().pin_memory(),
                      torch.empty(c.shape, dtype=c.dtype).pin_memory(), torch.empty(1, dtype=torch.float32).pin_memory()))
+        dev_in.append(tuple(torch.empty_like(t) if t.is_contiguous() else
+                            torch.empty_like(t.transpose(-1, -2).contiguous()).transpose(-1, -2)
+                            for t in (a, b, sa, sb)))
     h2d = sum(sum(t.numel() * t.element_size() for t in x[:4]) for x in host)
     d2h = sum(x[4].numel() * x[4].element_size() + 4 for x in host)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n_calls = len(ins)
+    comp_done = [None] * n_calls
+    out_done = [None] * n_calls
 
     def e2e_step():
-        for (ha, hb, hsa, hsb, hc, hm), (p, a, b, sa, sb, c, amax, kw) in zip(host, ins):
-            a.copy_(ha, non_blocking=True)
-            b.copy_(hb, non_blocking=True)
-            sa.copy_(hsa, non_blocking=True)
-            sb.copy_(hsb, non_blocking=True)
+        for i, ((ha, hb, hsa, hsb, hc, hm), (p, _, _, _, _, c, amax, kw)) in enumerate(zip(host, ins)):
+            a, b, sa, sb = dev_in[i]
+            with torch.cuda.stream(s_in):
+                if comp_done[i] is not None:
+                    s_in.wait_event(comp_done[i])   # the previous step's GEMM has read these operands
+                a.copy_(ha, non_blocking=True)
+                b.copy_(hb, non_blocking=True)
+                sa.copy_(hsa, non_blocking=True)
+                sb.copy_(hsb, non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            stream.wait_event(ready)
+            if out_done[i] is not None:
+                stream.wait_event(out_done[i])       # C of the previous step has been read back
             call((p, a, b, sa, sb, c, amax, kw))
-            hc.copy_(c, non_blocking=True)
-            hm.copy_(amax, non_blocking=True)
+            comp_done[i] = torch.cuda.Event()
+            comp_done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                hc.copy_(c, non_blocking=True)
+                hm.copy_(amax, non_blocking=True)
+                out_done[i] = torch.cuda.Event()
+                out_done[i].record(s_out)
 
     for _ in range(max(1, min(args.warmup, 3))):
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
     for _ in range(args.steps):
         e2e_step()
+    for ev in out_done:
+        stream.wait_event(ev)                      # every read-back is inside the timed region
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world, dev)

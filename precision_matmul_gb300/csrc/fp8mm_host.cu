@@ -296,14 +296,17 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   const bool auto_pair = d.cta_pair == 0 && !mx && !P->slow && !swap && P->Q > 128 &&
                          (d.block_n == 0 || (d.block_n == 224 && !mx) || d.block_n == 256) &&
                          pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
-  // Slow accumulation on CTA pairs (256-row held tiles of 224 or 256 columns)
-  // is built but only planned on request (cta_pair = 1): each 128-K chunk is
-  // handed from the pair's MMA to both CTAs' epilogues and back, and on GB300
-  // that round trip made every slow shape measured about 1.7-2x slower than
-  // one-CTA held tiles (4096^3: 146 vs 85 us), although each SM stages a
+  // Slow accumulation on CTA pairs: 256-row held tiles of 224 or 256
+  // columns.  Each 128-K chunk is handed from the pair's MMA to both CTAs'
+  // epilogues and back; with relaxed cluster-scope arrivals for the hand-back
+  // a pair's wave measured about 4% shorter than a one-CTA wave of the same
+  // width on GB300 (4096^3: 80.6 vs 82.6 us; 2048x28672x8192: 396 vs 411 us;
+  // 8192x7168x2048 with 128x128 scales: 167 vs 179 us), each SM staging a
   // third fewer operand bytes.  A 224-column tile's halves (112 columns per
   // epilogue warp) straddle 128-column scale blocks, so 128x128 Y scales
   // take 256.
+  constexpr double kSlowPairWave = 0.96;
+  bool slow_pair = false;
   const bool y_block128 = blockwise && P->y_kind == kScaleBlock128;
   if (bn == 0 && auto_pair) {
     // the width whose whole waves over the SM pairs cost least
@@ -333,6 +336,8 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
       // chunk's time follows its operand bytes (128 rows of X and BN of Y,
       // 128 bytes of K each), so the width with the fewest whole waves x
       // bytes per chunk wins; 128x128 Y scales need 128-aligned halves (256).
+      // Pair tiles compete with one-CTA tiles by the same measure, a pair's
+      // wave counted at kSlowPairWave of a one-CTA wave.
       bn = 128;
       if (!mx && d.splitk <= 1 && tiles_r1 * cdiv(P->Q, 256) * L >= (int64_t)P->sms) {
         double best = 1e300;
@@ -343,6 +348,15 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
           if (cost < best * 0.999) {
             best = cost;
             bn = c;
+            slow_pair = false;
+          }
+          if (c == 192 || d.cta_pair != 0) continue;  // pairs hold 224 or 256 columns
+          const int64_t ptiles = pair_rows * cdiv(P->Q, c) * L;
+          const double pcost = (double)cdiv(ptiles, P->sms / 2) * (kBlockM + c) * kSlowPairWave;
+          if (pcost < best * 0.999) {
+            best = pcost;
+            bn = c;
+            slow_pair = true;
           }
         }
       }
@@ -364,7 +378,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // Slow accumulation keeps the promoted sums in registers: 192, 224 or 256
   // columns on one CTA (224 and 256 on a CTA pair too), never swapped, split
   // or MX; 192/224 only where no 128x128 Y-scale block straddles a half.
-  const bool pair = d.cta_pair == 1 || auto_pair;
+  const bool pair = d.cta_pair == 1 || auto_pair || slow_pair;
   const bool slow_wide_ok = !swap && !mx && d.splitk <= 1 &&
                             (bn == 256 || ((bn == 224 || (bn == 192 && !pair)) && !y_block128));
   if (P->slow && bn > 128 && !slow_wide_ok) {
@@ -386,7 +400,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   }
   P->bn = bn;
 
-  if (d.cta_pair == 1 || auto_pair) {
+  if (pair) {
     if ((mx && !(mx_pairable && bn == 256)) || swap) return FP8MM_ERR_UNSUPPORTED;
     P->cg = 2;
   }

@@ -37,20 +37,21 @@ def test_llm_4096_fast_uses_pair_tiles(lib):
     assert i["units"] == 16 * 19 and i["stages"] == 6 and i["grid"] == SMS
 
 
-def test_llm_4096_slow_uses_held_224_column_tiles(lib):
-    # one-CTA held tiles: 32 x 19 = 608 tiles of 128 x 224, exactly four waves over 152 SMs
+def test_llm_4096_slow_uses_held_224_column_pair_tiles(lib):
+    # held pair tiles: 16 x 19 = 304 tiles of 256 x 224, exactly four waves over 76 SM pairs
     i = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0)
-    assert (i["cta_pair"], i["block_n"], i["splitk"], i["epi_warps"], i["slow"]) == (0, 224, 1, 8, 1)
-    assert i["stages"] == 4 and i["units"] == 32 * 19
-    # held slow tiles on CTA pairs only on request (measured slower)
-    j = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0, cta_pair=1, block_n=224)
-    assert (j["cta_pair"], j["block_n"], j["stages"], j["units"]) == (1, 224, 6, 16 * 19)
+    assert (i["cta_pair"], i["block_n"], i["splitk"], i["epi_warps"], i["slow"]) == (1, 224, 1, 8, 1)
+    assert i["stages"] == 6 and i["units"] == 16 * 19
+    # pairs off: one-CTA held tiles, 32 x 19 = 608 tiles of 128 x 224 (four waves over 152 SMs)
+    j = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0, cta_pair=2)
+    assert (j["cta_pair"], j["block_n"], j["stages"], j["units"]) == (0, 224, 4, 32 * 19)
 
 
 @pytest.mark.parametrize("mode,stages", [(B.FP8MM_SCALE_A1x128_B128x128, 3), (B.FP8MM_SCALE_A1x128_B1x128, 2)])
 def test_blockwise_shallow_ring(lib, mode, stages):
     i = preview(8192, 7168, 2048, out_dtype=1, scale_mode=mode, fast_accum=1)  # block scales are always slow
-    assert (i["block_n"], i["slow"], i["stages"], i["epi_warps"], i["cta_pair"]) == (256, 1, stages, 8, 0)
+    assert (i["block_n"], i["slow"], i["stages"], i["epi_warps"], i["cta_pair"]) == (256, 1, stages, 8, 1)
+    assert i["units"] == 32 * 28  # 256 x 256 pair tiles
 
 
 def test_mx_batched_held_256(lib):
@@ -64,8 +65,8 @@ def test_mx_batched_held_256(lib):
 
 @pytest.mark.parametrize("M,fast,swap,bn,splitk,pair", [
     (16, 1, 1, 16, 2, 0), (16, 0, 1, 16, 2, 0), (64, 1, 1, 64, 2, 0),
-    (256, 1, 0, 224, 1, 1), (256, 0, 0, 192, 1, 0), (1024, 0, 0, 256, 1, 0), (2048, 0, 0, 256, 1, 0),
-    (1024, 1, 0, 256, 1, 1), (2048, 1, 0, 256, 1, 1), (8192, 1, 0, 256, 1, 1), (8192, 0, 0, 256, 1, 0),
+    (256, 1, 0, 224, 1, 1), (256, 0, 0, 192, 1, 0), (1024, 0, 0, 256, 1, 1), (2048, 0, 0, 256, 1, 1),
+    (1024, 1, 0, 256, 1, 1), (2048, 1, 0, 256, 1, 1), (8192, 1, 0, 256, 1, 1), (8192, 0, 0, 256, 1, 1),
 ])
 def test_skinny_sweep(lib, M, fast, swap, bn, splitk, pair):
     i = preview(M, 28672, 8192, out_dtype=1, fast_accum=fast)
