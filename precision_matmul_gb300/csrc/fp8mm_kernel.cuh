@@ -444,8 +444,13 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   (void)ys_w;
   // The pair leader's accumulator-empty barrier collects both CTAs' warps.
   const uint32_t tempty_target = (CG == 2) ? ptx::mapa_shared(bar_tempty, 0u) : bar_tempty;
+  // Every TMEM read before a release went through tmem_load, whose
+  // tcgen05.wait::ld has the values in registers, so nothing the next MMA
+  // writes can reach them.  One CTA keeps the tcgen05 fence before the arrive
+  // (it costs nothing there); on a CTA pair it measured ~70 cycles per chunk
+  // of the hand-off on GB300, and is left out.
   auto release_acc = [&]() {
-    ptx::tc_fence_before_sync();
+    if constexpr (CG == 1) ptx::tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) {
       if constexpr (CG == 2)
