@@ -132,7 +132,8 @@ size_t layout(fp8mm_plan_s* P, int stages) {
   off += sf_bytes * stages;
   off = (off + 1023u) & ~1023u;
   P->off_out = off;
-  off += (uint32_t)(P->ew * stage_out_bytes(P->ew, held_tile(P->bn, P->slow != 0, P->mx != 0)));
+  off += (uint32_t)(P->ew * stage_out_bytes(P->ew, held_tile(P->bn, P->slow != 0, P->mx != 0), P->out_es,
+                                             part_max_cols(P->bn, P->ew, P->slow != 0)));
   P->off_ys = off;
   // per-column Y scales of the current chunk, one row per epilogue warp
   if (P->x_kind != kScaleNone && P->y_kind == kScaleRow) off += (uint32_t)(P->ew * part_max_cols(P->bn, P->ew, P->slow != 0) * 4);

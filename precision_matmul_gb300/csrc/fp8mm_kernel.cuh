@@ -84,7 +84,12 @@ __host__ __device__ constexpr bool held_tile(int bn, bool slow, bool mx) {
 // or 32 rows x 32 B (16 epilogue warps, or held tiles, whose registers leave
 // less room).  (Rows of 16 B measured far slower: the stores then write half
 // sectors.)
-__host__ __device__ constexpr int stage_out_bytes(int ew, bool held) { return (ew == 8 && !held) ? 4096 : 2048; }
+// Output staging per epilogue warp.  Held tiles with 1- or 2-byte outputs
+// stage the warp's whole 32 x hmax block (all its chunks at once, stored
+// without waiting between them); the others alternate two chunk buffers.
+__host__ __device__ constexpr int stage_out_bytes(int ew, bool held, int es = 4, int hmax = 0) {
+  return held ? (es <= 2 ? 32 * hmax * es : 2048) : (ew == 8 ? 4096 : 2048);
+}
 // Columns [0, half0_cols) belong to epilogue warps 0-3, the rest to warps 4-7
 // (slow 224- and 256-column tiles split evenly: every warp promotes as many
 // columns as its neighbour).
@@ -275,8 +280,10 @@ __device__ __forceinline__ float bias_at(const KParams& p, int n) {
 // first CW); NOSWAP drops the transposed staging of swapped operands.
 // With a bias, bias_cols points at the chunk's CW bias values staged in
 // shared memory (unswapped tiles; 0 past the last column) and bias_lane holds
-// the thread's own column's value (swapped tiles).
-template <int CW, int ES, int NV, bool NOSWAP = false>
+// the thread's own column's value (swapped tiles).  STREAM: the caller has
+// made the buffer free and commits the bulk group after its last chunk (a
+// held tile's chunks go out back to back).
+template <int CW, int ES, int NV, bool NOSWAP = false, bool STREAM = false>
 __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap* tm_c, float (&v)[NV], float alpha,
                                             float sr, const float* bias_cols, float bias_lane, bool row_ok, int q0,
                                             int lane, uint8_t* stg_gen, uint32_t stg_s, int cx, int cy, int cl,
@@ -304,8 +311,10 @@ __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap*
     for (int i = 0; i < CW; ++i) m = max_nan(m, (q0 + i < p.Q) ? fabsf(v[i]) : 0.0f);
   }
   const bool has_nan = m != m;
-  if (lane == 0) ptx::bulk_wait_read_one();  // this buffer's previous store has read it
-  __syncwarp();
+  if constexpr (!STREAM) {
+    if (lane == 0) ptx::bulk_wait_read_one();  // this buffer's previous store has read it
+    __syncwarp();
+  }
   if constexpr (ES == 1) {
     // FP8 output: amax of the fp32 values before scale_result (it sets the
     // next quantisation scale), then one saturating rounding of v * sr.
@@ -387,7 +396,7 @@ __device__ __forceinline__ void store_chunk(const KParams& p, const CUtensorMap*
   // past its end holds nothing to store and is skipped (no group is committed).
   if (lane == 0) {
     if (in_bounds) ptx::tma_store_3d(tm_c, stg_s, cx, cy, cl);
-    ptx::bulk_commit();
+    if constexpr (!STREAM) ptx::bulk_commit();
   }
 }
 
@@ -410,7 +419,15 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
   static_assert(EW == 8 || BN % 128 == 0, "16 epilogue warps split 128-multiple tiles in four");
   static_assert(!SLOW || HMAX * (EW / 4) == BN, "slow accumulation splits the tile evenly");
   static_assert(HMAX % CW == 0 && (BN - HMAX) % CW == 0, "chunks tile each part");
-  constexpr int kStageOut = stage_out_bytes(EW, HOLD);
+  constexpr int kStageOut = stage_out_bytes(EW, HOLD, ES, HMAX);
+  // Held tiles with 1- or 2-byte outputs stage all of a warp's chunks at once
+  // and store them back to back: with two alternating buffers each chunk
+  // waited for the TMA unit to read the one before last, and on GB300 a held
+  // 128 x 256 tile's stores took about 19,000 cycles, during which the MMA
+  // could run only two chunks ahead.
+  constexpr bool kWhole = HOLD && ES <= 2;
+  constexpr int kChunkBytes = 32 * CW * ES;
+  static_assert(!kWhole || kStageOut == (HMAX / CW) * kChunkBytes, "a whole block of chunks");
   const int qd = warp & 3;
   const int h = warp >> 2;
   const int row = qd * 32 + lane;
@@ -717,8 +734,25 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
           bias_lane = bias_at(p, xr);
         }
       }
+      if constexpr (kWhole) {
+        // the previous tile's stores have read the staging block
+        if (lane == 0) ptx::bulk_wait_read_all();
+        __syncwarp();
+      }
       auto finish_chunk = [&](int ci) {
-        if constexpr (HOLD) {
+        if constexpr (kWhole) {
+          // The held sums are stored in place: the chunk is acc[0 .. CW),
+          // then the others move down by CW.  Chunk ci has its own slot.
+          const int q0 = t.tq * BN + col0 + ci * CW;
+          float v[CW];
+#pragma unroll
+          for (int i = 0; i < CW; ++i) v[i] = acc(i);
+          store_chunk<CW, ES, CW, true, true>(p, tm_c, v, alpha, sr, bias_w + ci * CW, bias_lane, row_ok, q0, lane,
+                                                stg + ci * kChunkBytes, stg_s + ci * kChunkBytes, q0, r0, t.l,
+                                                q0 < p.Q && r0 < p.R, amax_f, amax_nan);
+#pragma unroll
+          for (int i = 0; i < (HMAX - CW) / 2; ++i) acc2[i] = acc2[i + CW / 2];
+        } else if constexpr (HOLD) {
           // The held sums are stored in place: the chunk is acc[0 .. CW),
           // then the others move down by CW.
           const int q0 = t.tq * BN + col0 + ci * CW;
@@ -770,6 +804,9 @@ __device__ __forceinline__ void epilogue(const KParams& p, const CUtensorMap* tm
       };
 #pragma unroll 1
       for (int ci = 0; ci < nch; ++ci) finish_chunk(ci);
+      if constexpr (kWhole) {
+        if (lane == 0) ptx::bulk_commit();
+      }
     }
     if constexpr (!SLOW && !HOLD) release_acc();
   }
