@@ -64,6 +64,28 @@ def test_fp8_out_slow_held_tiles(block_n):
     _run_check(p, scale_result=16.0, block_n=block_n, cta_pair=1 if block_n == 224 else 2, swap_ab=2)
 
 
+@pytest.mark.parametrize("tile", [(2, 192), (2, 224), (2, 256), (1, 224), (1, 256)])
+@pytest.mark.parametrize("form", ["bf16_bias", "f16", "e4m3"])
+def test_held_tiles_several_per_cta(tile, form):
+    # Held slow tiles with 1- or 2-byte outputs stage a warp's whole block and
+    # store its chunks back to back; with more tiles than SMs (or SM pairs) each
+    # CTA reuses that staging for its next tile.  Ragged in M, N and K.
+    pair, block_n = tile
+    if form == "e4m3":
+        p = _fp8_problem(synth.OUT_E4M3, fast=False, M=1000, N=2608, K=400, seed=64, L=2)
+        kw = dict(scale_result=0.75)
+    else:
+        out = synth.OUT_BF16 if form == "bf16_bias" else synth.OUT_F16
+        p = synth.llm_per_tensor(L=2, M=1000, N=2608, K=400, seed=65, fast_accum=False, out_dtype=out)
+        p.scale_a.fill_(0.0625)
+        p.scale_b.fill_(0.5)
+        kw = dict(bias=_bias(p, 68)) if form == "bf16_bias" else {}
+    c, amax, plan = _run_check(p, block_n=block_n, cta_pair=pair, swap_ab=2, **kw)
+    info = plan.info()
+    assert (info["block_n"], info["cta_pair"], info["splitk"]) == (block_n, 1 if pair == 1 else 0, 1)
+    assert info["units"] > (76 if pair == 1 else 152)
+
+
 def test_fp8_out_blockwise_and_mx():
     p = synth.blockwise(M=272, N=400, K=640, seed=63, out_dtype=synth.OUT_E4M3)
     p.scale_a.mul_(2.0 ** -16)
