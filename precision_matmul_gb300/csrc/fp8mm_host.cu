@@ -747,7 +747,7 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
   }
   // One TMA store per warp covers 32 tile rows x `cw` tile columns, staged in
   // shared memory with the swizzle that matches its row length.
-  const int cw = chunk_cols(P->bn, P->out_es, P->ew, held_tile(P->bn, P->slow != 0, P->mx != 0));
+  const int cw = chunk_cols(P->bn, P->out_es, P->ew, held_tile(P->bn, P->slow != 0, P->mx != 0), P->slow != 0);
   uint32_t rowbytes;
   cuuint32_t cbox[3];
   if (!P->swap) {

@@ -100,11 +100,17 @@ __host__ __device__ constexpr int half0_cols(int bn, bool slow = false) {
 __host__ __device__ constexpr int part_max_cols(int bn, int ew, bool slow = false) {
   return ew == 8 ? half0_cols(bn, slow) : bn / 4;
 }
-// Columns of one output chunk (one TMA store of 32 tile rows).
-// FP8 outputs use rows of 32 bytes (16 for held tiles, whose 112-column
-// parts are not multiples of 32).
-__host__ __device__ constexpr int chunk_cols(int bn, int es, int ew, bool held) {
-  return held ? (es == 1 ? 16 : 32 / es)
+// Columns of one output chunk (one TMA store of 32 tile rows).  Held tiles
+// with 1- or 2-byte outputs take the widest of 64, 32 and 16 columns that
+// divides both warps' parts (256-, 192- and 224-column slow tiles); fp32
+// outputs 8.
+__host__ __device__ constexpr int chunk_cols(int bn, int es, int ew, bool held, bool slow = false) {
+  return held ? (es == 4 ? 8
+                         : (part_max_cols(bn, ew, slow) % 64 == 0 && (bn - part_max_cols(bn, ew, slow)) % 64 == 0)
+                               ? 64
+                               : (part_max_cols(bn, ew, slow) % 32 == 0 && (bn - part_max_cols(bn, ew, slow)) % 32 == 0)
+                                     ? 32
+                                     : 16)
          : es == 1 ? (32 < part_max_cols(bn, ew) ? 32 : part_max_cols(bn, ew))
                    : (((ew == 8 ? 64 : 32) / es) < part_max_cols(bn, ew) ? ((ew == 8 ? 64 : 32) / es)
                                                                           : part_max_cols(bn, ew));
@@ -216,7 +222,12 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
 
 template <int N>
 __device__ __forceinline__ void tmem_load(uint32_t taddr, uint32_t (&r)[N]) {
-  if constexpr (N == 32) {
+  if constexpr (N == 64) {
+    ptx::tmem_ld_32x32b_x32(taddr, reinterpret_cast<uint32_t(&)[32]>(r[0]));
+    ptx::tmem_ld_32x32b_x32(taddr + 32, reinterpret_cast<uint32_t(&)[32]>(r[32]));
+    ptx::tmem_ld_wait_x32(reinterpret_cast<uint32_t(&)[32]>(r[0]));
+    ptx::tmem_ld_wait_x32(reinterpret_cast<uint32_t(&)[32]>(r[32]));
+  } else if constexpr (N == 32) {
     ptx::tmem_ld_32x32b_x32(taddr, r);
     ptx::tmem_ld_wait_x32(r);
   } else if constexpr (N == 16) {
@@ -862,7 +873,7 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
   }
   // FP8 outputs store rows of at least 16 bytes starting on 16-byte columns
   // (a TMA store's rule): unswapped tiles need chunks of 16 columns or more.
-  if (p.out_es == 1 && !p.swap && chunk_cols(BN, 1, EW, held_tile(BN, SLOW, MX)) < 16) {
+  if (p.out_es == 1 && !p.swap && chunk_cols(BN, 1, EW, held_tile(BN, SLOW, MX), SLOW) < 16) {
     if (threadIdx.x == 0) atomicOr(p.abort_word, kErrPlan);
     return;
   }
@@ -1177,15 +1188,15 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
     // ------------------------------------------------------------ epilogue
     if constexpr (REGSPLIT) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(epi_regs(EW)));
     if (p.out_es == 4)
-      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 4, EW, held_tile(BN, SLOW, MX)), 4, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 4, EW, held_tile(BN, SLOW, MX), SLOW), 4, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
                                                             lane);
     else if (p.out_es == 1)
-      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 1, EW, held_tile(BN, SLOW, MX)), 1, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 1, EW, held_tile(BN, SLOW, MX), SLOW), 1, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
                                                             lane);
     else
-      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 2, EW, held_tile(BN, SLOW, MX)), 2, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
+      epilogue<BN, SLOW, CG, EW, chunk_cols(BN, 2, EW, held_tile(BN, SLOW, MX), SLOW), 2, held_tile(BN, SLOW, MX)>(p, &tm_c, sgen, sbase, tmem_base, bar_tfull, bar_tempty,
                                                             bar_epi, misc, abort_flag, rank, u_first, u_step, warp,
                                                             lane);
   } else {
