@@ -127,9 +127,11 @@ typedef struct {
   int32_t splitk;      /* 0: choose; S >= 1: split K into S contiguous 128-aligned ranges */
   int32_t swap_ab;     /* 0: choose; 1: force on; 2: force off */
   int32_t block_n;     /* 0: choose; else the tile width on the MMA's N side, one the library
-                          instantiates: fast 16, 32, 64, 128, 192, 224, 256 (CTA pairs 128, 224,
-                          256); slow 16, 32, 64, 128 (CTA pairs 128) and 256 (unswapped, one
-                          CTA); MX 128, 224, 256 (slow MX 128).  Others: FP8MM_ERR_UNSUPPORTED. */
+                          instantiates: fast 16, 32, 64, 128, 192, 224, 256 (CTA pairs 128, 192,
+                          224, 256); slow 16, 32, 64, 128 (CTA pairs 128) and, unswapped and
+                          unsplit, 192, 224, 256 on one CTA or a CTA pair (192/224 not with
+                          128x128 B scales); MX 128, 224, 256 (CTA pairs 256, slow MX 128); FP4
+                          128, 256.  Others: FP8MM_ERR_UNSUPPORTED. */
   int32_t device;      /* CUDA device ordinal the plan is for */
   int32_t cta_pair;    /* two-SM (CTA pair) tiles: 0 choose; 1 force on; 2 force off */
   int32_t epi_warps;   /* epilogue warps per CTA: 0 choose, 8 or 16 */

@@ -295,9 +295,9 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // 237 us), whose time per stage they share.
   const bool mx_pairable = mx && !f4 && !P->slow;
   const bool auto_pair = d.cta_pair == 0 && !mx && !P->slow && !swap && P->Q > 128 &&
-                         (d.block_n == 0 || (d.block_n == 224 && !mx) || d.block_n == 256) &&
+                         (d.block_n == 0 || ((d.block_n == 224 || d.block_n == 192) && !mx) || d.block_n == 256) &&
                          pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
-  // Slow accumulation on CTA pairs: 256-row held tiles of 224 or 256
+  // Slow accumulation on CTA pairs: 256-row held tiles of 192, 224 or 256
   // columns.  Each 128-K chunk is handed from the pair's MMA to both CTAs'
   // epilogues and back; with relaxed cluster-scope arrivals for the hand-back
   // a pair's wave measured about 4% shorter than a one-CTA wave of the same
@@ -312,7 +312,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   if (bn == 0 && auto_pair) {
     // the width whose whole waves over the SM pairs cost least
     double best = 1e300;
-    for (int c : {256, 224}) {
+    for (int c : {256, 224, 192}) {
       if (mx && c != 256) continue;
       const int64_t tiles = pair_rows * cdiv(P->Q, c) * L;
       const double cost = (double)cdiv(tiles, P->sms / 2) * c / width_efficiency(c, false);
@@ -351,7 +351,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
             bn = c;
             slow_pair = false;
           }
-          if (c == 192 || d.cta_pair != 0) continue;  // pairs hold 224 or 256 columns
+          if (d.cta_pair != 0) continue;
           const int64_t ptiles = pair_rows * cdiv(P->Q, c) * L;
           const double pcost = (double)cdiv(ptiles, P->sms / 2) * (kBlockM + c) * kSlowPairWave;
           if (pcost < best * 0.999) {
@@ -377,11 +377,11 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
     }
   }
   // Slow accumulation keeps the promoted sums in registers: 192, 224 or 256
-  // columns on one CTA (224 and 256 on a CTA pair too), never swapped, split
-  // or MX; 192/224 only where no 128x128 Y-scale block straddles a half.
+  // columns, on one CTA or a CTA pair, never swapped, split or MX; 192/224
+  // only where no 128x128 Y-scale block straddles a half.
   const bool pair = d.cta_pair == 1 || auto_pair || slow_pair;
   const bool slow_wide_ok = !swap && !mx && d.splitk <= 1 &&
-                            (bn == 256 || ((bn == 224 || (bn == 192 && !pair)) && !y_block128));
+                            (bn == 256 || ((bn == 224 || bn == 192) && !y_block128));
   if (P->slow && bn > 128 && !slow_wide_ok) {
     if (d.block_n != 0) return FP8MM_ERR_UNSUPPORTED;
     bn = 128;

@@ -26,6 +26,7 @@ KernelFn kernel_bn224_fast_f8_cg1_ew8();
 KernelFn kernel_bn256_fast_f8_cg1_ew8();
 KernelFn kernel_bn256_fast_f8_cg2_ew8();
 KernelFn kernel_bn224_fast_f8_cg2_ew8();
+KernelFn kernel_bn192_fast_f8_cg2_ew8();
 KernelFn kernel_bn128_fast_f8_cg2_ew8();
 KernelFn kernel_bn128_slow_f8_cg2_ew8();
 KernelFn kernel_bn128_slow_f8_cg1_ew8();
@@ -36,6 +37,7 @@ KernelFn kernel_bn256_slow_f8_cg2_ew8();
 KernelFn kernel_bn224_slow_f8_cg1_ew8();
 KernelFn kernel_bn192_slow_f8_cg1_ew8();
 KernelFn kernel_bn224_slow_f8_cg2_ew8();
+KernelFn kernel_bn192_slow_f8_cg2_ew8();
 KernelFn kernel_bn128_fast_mx_cg1_ew8();
 KernelFn kernel_bn224_fast_mx_cg1_ew8();
 KernelFn kernel_bn256_fast_mx_cg1_ew8();
@@ -63,6 +65,7 @@ inline const KernelEntry* kernel_table(int* n) {
       {256, 0, 0, 1, 8, 0, &kernel_bn256_fast_f8_cg1_ew8},
       {256, 0, 0, 2, 8, 0, &kernel_bn256_fast_f8_cg2_ew8},
       {224, 0, 0, 2, 8, 0, &kernel_bn224_fast_f8_cg2_ew8},
+      {192, 0, 0, 2, 8, 0, &kernel_bn192_fast_f8_cg2_ew8},
       {128, 0, 0, 2, 8, 0, &kernel_bn128_fast_f8_cg2_ew8},
       {128, 1, 0, 2, 8, 0, &kernel_bn128_slow_f8_cg2_ew8},
       {128, 1, 0, 1, 8, 0, &kernel_bn128_slow_f8_cg1_ew8},
@@ -73,6 +76,7 @@ inline const KernelEntry* kernel_table(int* n) {
       {224, 1, 0, 1, 8, 0, &kernel_bn224_slow_f8_cg1_ew8},
       {192, 1, 0, 1, 8, 0, &kernel_bn192_slow_f8_cg1_ew8},
       {224, 1, 0, 2, 8, 0, &kernel_bn224_slow_f8_cg2_ew8},
+      {192, 1, 0, 2, 8, 0, &kernel_bn192_slow_f8_cg2_ew8},
       {128, 0, 1, 1, 8, 0, &kernel_bn128_fast_mx_cg1_ew8},
       {224, 0, 1, 1, 8, 0, &kernel_bn224_fast_mx_cg1_ew8},
       {256, 0, 1, 1, 8, 0, &kernel_bn256_fast_mx_cg1_ew8},

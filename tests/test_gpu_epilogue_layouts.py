@@ -64,7 +64,7 @@ def test_fp8_out_slow_held_tiles(block_n):
     _run_check(p, scale_result=16.0, block_n=block_n, cta_pair=1 if block_n == 224 else 2, swap_ab=2)
 
 
-@pytest.mark.parametrize("tile", [(2, 192), (2, 224), (2, 256), (1, 224), (1, 256)])
+@pytest.mark.parametrize("tile", [(2, 192), (2, 224), (2, 256), (1, 192), (1, 224), (1, 256)])
 @pytest.mark.parametrize("form", ["bf16_bias", "f16", "e4m3"])
 def test_held_tiles_several_per_cta(tile, form):
     # Held slow tiles with 1- or 2-byte outputs stage a warp's whole block and

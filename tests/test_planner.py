@@ -69,7 +69,7 @@ def test_mx_batched_held_256(lib):
 
 @pytest.mark.parametrize("M,fast,swap,bn,splitk,pair", [
     (16, 1, 1, 16, 2, 0), (16, 0, 1, 16, 2, 0), (64, 1, 1, 64, 2, 0),
-    (256, 1, 0, 224, 1, 1), (256, 0, 0, 192, 1, 0), (1024, 0, 0, 256, 1, 1), (2048, 0, 0, 256, 1, 1),
+    (256, 1, 0, 192, 1, 1), (256, 0, 0, 192, 1, 1), (1024, 0, 0, 256, 1, 1), (2048, 0, 0, 256, 1, 1),
     (1024, 1, 0, 256, 1, 1), (2048, 1, 0, 256, 1, 1), (8192, 1, 0, 256, 1, 1), (8192, 0, 0, 256, 1, 1),
 ])
 def test_skinny_sweep(lib, M, fast, swap, bn, splitk, pair):
@@ -92,7 +92,8 @@ def test_workspace_free_plans_have_no_split(lib):
     (dict(block_n=256, fast_accum=0, epi_warps=16), B.FP8MM_OK),
     (dict(block_n=224, fast_accum=0, cta_pair=1), B.FP8MM_OK),                       # held slow pair tile
     (dict(block_n=224, fast_accum=0, cta_pair=2), B.FP8MM_OK),                      # 224 held on one CTA
-    (dict(block_n=192, fast_accum=0, cta_pair=1), B.FP8MM_ERR_UNSUPPORTED),         # 192 held on one CTA only
+    (dict(block_n=192, fast_accum=0, cta_pair=1), B.FP8MM_OK),                       # 192 held on a pair
+    (dict(block_n=192, cta_pair=1, scale_mode=B.FP8MM_SCALE_A1x128_B128x128), B.FP8MM_ERR_UNSUPPORTED),
     (dict(block_n=224, cta_pair=1, scale_mode=B.FP8MM_SCALE_A1x128_B128x128), B.FP8MM_ERR_UNSUPPORTED),
     (dict(block_n=224, cta_pair=1, scale_mode=B.FP8MM_SCALE_A1x128_B1x128), B.FP8MM_OK),
     (dict(block_n=256, fast_accum=0, cta_pair=1, epi_warps=16), B.FP8MM_ERR_UNSUPPORTED),
