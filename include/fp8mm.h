@@ -230,6 +230,15 @@ const char* fp8mm_status_string(fp8mm_status status);
  * on `device` has aborted since the last clear.  Synchronises the device. */
 fp8mm_status fp8mm_device_error(int device, uint32_t* code, int clear);
 
+/* Test support for the abort path.  While enabled (process-wide), GEMM kernels
+ * launched afterwards issue no operand loads, so the MMA issuer's first wait
+ * for a stage, and the epilogue's for the accumulator, never complete: the
+ * first to reach its limit (2^31 SM cycles, about one second) records a
+ * nonzero code in the abort word (fp8mm_device_error), and every role of the
+ * kernel drains and returns; the CUDA context stays usable.  The outputs of
+ * such calls are undefined.  Not for use outside tests. */
+fp8mm_status fp8mm_test_withhold_loads(int enable);
+
 /* Number of kernel launches fp8mm_run enqueues for this plan (the amax reset
  * and, with split-K, the counter reset are stream memsets, not kernels). */
 fp8mm_status fp8mm_plan_kernel_launches(const fp8mm_plan_t* plan, int32_t* launches);

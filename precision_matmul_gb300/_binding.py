@@ -25,7 +25,7 @@ FP8MM_ERR_REJECTED, FP8MM_ERR_WORKSPACE, FP8MM_ERR_CUDA, FP8MM_ERR_DEVICE = 4, 5
 EXPORTS = ("fp8mm_plan", "fp8mm_workspace_size", "fp8mm_run", "fp8mm_plan_roofline",
            "fp8mm_plan_get_info", "fp8mm_destroy", "fp8mm_status_string", "fp8mm_device_error",
            "fp8mm_plan_kernel_launches", "fp8mm_gemm", "fp8mm_run_static_workspace", "fp8mm_plan_preview",
-           "fp8mm_run_ex")
+           "fp8mm_run_ex", "fp8mm_test_withhold_loads")
 FP8MM_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 
@@ -90,6 +90,8 @@ def load():
     lib.fp8mm_plan_preview.argtypes = [ctypes.POINTER(fp8mm_desc), i32, i32, ctypes.POINTER(fp8mm_plan_info)]
     lib.fp8mm_plan_preview.restype = i32
     lib.fp8mm_run_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.fp8mm_test_withhold_loads.argtypes = [i32]
+    lib.fp8mm_test_withhold_loads.restype = i32
     lib.fp8mm_run_ex.restype = i32
     _lib = lib
     return lib
@@ -188,6 +190,12 @@ def fp8mm_device_error(device: int = 0, clear: bool = True) -> int:
     code = ctypes.c_uint32()
     _check(load().fp8mm_device_error(int(device), ctypes.byref(code), int(bool(clear))), "fp8mm_device_error")
     return int(code.value)
+
+
+def fp8mm_test_withhold_loads(enable: bool) -> None:
+    """Test support: GEMM kernels launched while enabled issue no operand loads,
+    so their MMA issuer's wait runs out and the kernel aborts (see the header)."""
+    _check(load().fp8mm_test_withhold_loads(1 if enable else 0), "fp8mm_test_withhold_loads")
 
 
 def fp8mm_gemm(desc: fp8mm_desc, a_ptr, b_ptr, sa_ptr, sb_ptr, c_ptr, amax_ptr, ws_ptr=None, ws_bytes=0,

@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -161,7 +162,16 @@ double width_efficiency(int bn, bool mx) {
 
 }  // namespace
 
+namespace {
+std::atomic<int> g_withhold_loads{0};  // fp8mm_test_withhold_loads
+}  // namespace
+
 extern "C" {
+
+fp8mm_status fp8mm_test_withhold_loads(int enable) {
+  g_withhold_loads.store(enable ? 1 : 0);
+  return FP8MM_OK;
+}
 
 const char* fp8mm_status_string(fp8mm_status s) {
   switch (s) {
@@ -795,6 +805,7 @@ fp8mm_status fp8mm_run_ex(fp8mm_plan_t* P, const void* a, const void* b, const v
   kp.group = P->group;
   kp.units = P->units;
   kp.swap = P->swap;
+  kp.withhold_loads = g_withhold_loads.load() ? 1 : 0;
   kp.out_dtype = d.out_dtype;
   kp.out_es = P->out_es;
   kp.scale_result = scale_result;

@@ -135,6 +135,7 @@ struct KParams {
   int group;              // tile rows per raster group
   long long units;        // L * tiles_r * tiles_q * splits
   int swap;               // 1: C[m][n] is tile(q = m, r = n)
+  int withhold_loads;     // abort-path test: the producer issues nothing, so the MMA issuer's wait runs out
   int out_dtype;          // 0 f32, 1 bf16, 2 f16, 3 E4M3, 4 E5M2
   int out_es;             // bytes per output element
   const float* scale_result;  // FP8 outputs: multiplies the result before the FP8 rounding (device), or null
@@ -939,7 +940,7 @@ __global__ void __launch_bounds__(kernel_threads(EW, held_tile(BN, SLOW, MX)), 1
       }
       uint32_t stage = 0, phase = 0;
       long long narm = 0;
-      bool ok = true;
+      bool ok = !p.withhold_loads;
       // With a CTA pair both CTAs' copies complete on the leader's full barrier,
       // which the leader arms with the bytes of both.
       for (long long u = u_first; ok && u < p.units; u += u_step) {
