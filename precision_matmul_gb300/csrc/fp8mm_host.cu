@@ -300,10 +300,15 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // GB300 for fast unswapped GEMMs with at least one wave of pairs.
   const int64_t pair_rows = std::max<int64_t>(1, cdiv(P->R, 2 * kBlockM));
   // MX (FP8 operands) pairs: 256-column tiles only, each CTA staging its own
-  // rows' factor atom and all of the Y tile's.  Planned only on request: on
-  // GB300 they measured no faster than one-CTA held tiles (4 x 4096^3: 246 vs
-  // 237 us), whose time per stage they share.
+  // rows' factor atom and all of the Y tile's.  With 1- or 2-byte outputs
+  // (whose held tiles stage a whole block per warp and store it back to back)
+  // they measured faster than one-CTA held tiles on GB300: 4 x 4096^3 bf16 out
+  // 212 against 224 us; with fp32 outputs both took 233-235 us, so those keep
+  // one CTA.
   const bool mx_pairable = mx && !f4 && !P->slow;
+  const bool auto_mx_pair = d.cta_pair == 0 && mx_pairable && !swap && P->out_es <= 2 && d.splitk <= 1 &&
+                            (d.block_n == 0 || d.block_n == 256) &&
+                            pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
   const bool auto_pair = d.cta_pair == 0 && !mx && !P->slow && !swap && P->Q > 128 &&
                          (d.block_n == 0 || ((d.block_n == 224 || d.block_n == 192) && !mx) || d.block_n == 256) &&
                          pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
@@ -319,6 +324,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   constexpr double kSlowPairWave = 0.96;
   bool slow_pair = false;
   const bool y_block128 = blockwise && P->y_kind == kScaleBlock128;
+  if (bn == 0 && auto_mx_pair) bn = 256;
   if (bn == 0 && auto_pair) {
     // the width whose whole waves over the SM pairs cost least
     double best = 1e300;
@@ -389,7 +395,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // Slow accumulation keeps the promoted sums in registers: 192, 224 or 256
   // columns, on one CTA or a CTA pair, never swapped, split or MX; 192/224
   // only where no 128x128 Y-scale block straddles a half.
-  const bool pair = d.cta_pair == 1 || auto_pair || slow_pair;
+  const bool pair = d.cta_pair == 1 || auto_pair || slow_pair || auto_mx_pair;
   const bool slow_wide_ok = !swap && !mx && d.splitk <= 1 &&
                             (bn == 256 || ((bn == 224 || bn == 192) && !y_block128));
   if (P->slow && bn > 128 && !slow_wide_ok) {
