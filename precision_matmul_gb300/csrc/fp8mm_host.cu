@@ -300,13 +300,12 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   // GB300 for fast unswapped GEMMs with at least one wave of pairs.
   const int64_t pair_rows = std::max<int64_t>(1, cdiv(P->R, 2 * kBlockM));
   // MX (FP8 operands) pairs: 256-column tiles only, each CTA staging its own
-  // rows' factor atom and all of the Y tile's.  With 1- or 2-byte outputs
-  // (whose held tiles stage a whole block per warp and store it back to back)
-  // they measured faster than one-CTA held tiles on GB300: 4 x 4096^3 bf16 out
-  // 212 against 224 us; with fp32 outputs both took 233-235 us, so those keep
-  // one CTA.
+  // rows' factor atom and all of the Y tile's.  Once held tiles stored wider
+  // chunks (a whole block per warp for 1- and 2-byte outputs, 16 columns for
+  // fp32) they measured faster than one-CTA held tiles on GB300: 4 x 4096^3
+  // bf16 out 212 against 224 us, fp32 out 224 against 233 us.
   const bool mx_pairable = mx && !f4 && !P->slow;
-  const bool auto_mx_pair = d.cta_pair == 0 && mx_pairable && !swap && P->out_es <= 2 && d.splitk <= 1 &&
+  const bool auto_mx_pair = d.cta_pair == 0 && mx_pairable && !swap && d.splitk <= 1 &&
                             (d.block_n == 0 || d.block_n == 256) &&
                             pair_rows * cdiv(P->Q, 256) * L >= (int64_t)(P->sms / 2);
   const bool auto_pair = d.cta_pair == 0 && !mx && !P->slow && !swap && P->Q > 128 &&

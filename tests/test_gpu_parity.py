@@ -355,6 +355,17 @@ def test_mx_pair_tiles(fmt, out):
     assert (info["block_n"], info["cta_pair"]) == (256, 1)
 
 
+@pytest.mark.parametrize("fmt", [synth.E4M3, synth.E5M2])
+@pytest.mark.parametrize("out", [synth.OUT_F32, synth.OUT_BF16])
+def test_mx_one_cta_held_tiles(fmt, out):
+    # the one-CTA MX form (128 x 256 held tiles, one accumulator), now planned only
+    # with pairs off; ragged in M, N and K over a batch of two, several tiles per CTA
+    p = synth.mx_batched(L=2, M=1288, N=2600, K=416, fmt=fmt, seed=54, out_dtype=out)
+    c, amax, plan = _run_check(p, block_n=256, cta_pair=2)
+    info = plan.info()
+    assert (info["block_n"], info["cta_pair"]) == (256, 0) and info["units"] > 152
+
+
 def test_mx_pair_tiles_multiwave_with_fp8_output():
     p = synth.mx_batched(L=3, M=1024, N=2304, K=512, seed=53, out_dtype=synth.OUT_E4M3)
     p.scale_a.fill_(127 - 8)

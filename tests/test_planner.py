@@ -59,12 +59,13 @@ def test_blockwise_shallow_ring(lib, mode, stages):
 
 
 def test_mx_batched_held_256(lib):
+    # 256 x 256 held tiles on CTA pairs, 5 stages of 34 KiB per SM beside the fp32 output staging
     i = preview(4096, 4096, 4096, 4, scale_mode=B.FP8MM_SCALE_MX32_UE8M0, out_dtype=0, fast_accum=1)
-    assert (i["block_n"], i["cta_pair"], i["splitk"], i["stages"]) == (256, 0, 1, 4)
-    assert i["units"] == 4 * 32 * 16
-    # on request: 256 x 256 held tiles on CTA pairs, 6 stages of 34 KiB per SM
-    j = preview(4096, 4096, 4096, 4, scale_mode=B.FP8MM_SCALE_MX32_UE8M0, out_dtype=0, fast_accum=1, cta_pair=1)
-    assert (j["block_n"], j["cta_pair"], j["stages"], j["units"]) == (256, 1, 6, 4 * 16 * 16)
+    assert (i["block_n"], i["cta_pair"], i["splitk"], i["stages"]) == (256, 1, 1, 5)
+    assert i["units"] == 4 * 16 * 16
+    # pairs off: 128 x 256 held tiles on one CTA, 3 stages of 50 KiB
+    j = preview(4096, 4096, 4096, 4, scale_mode=B.FP8MM_SCALE_MX32_UE8M0, out_dtype=0, fast_accum=1, cta_pair=2)
+    assert (j["block_n"], j["cta_pair"], j["stages"], j["units"]) == (256, 0, 3, 4 * 32 * 16)
 
 
 @pytest.mark.parametrize("M,fast,swap,bn,splitk,pair", [
