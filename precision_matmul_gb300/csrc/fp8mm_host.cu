@@ -353,14 +353,20 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
       // 128 bytes of K each), so the width with the fewest whole waves x
       // bytes per chunk wins; 128x128 Y scales need 128-aligned halves (256).
       // Pair tiles compete with one-CTA tiles by the same measure, a pair's
-      // wave counted at kSlowPairWave of a one-CTA wave.
+      // wave counted at kSlowPairWave of a one-CTA wave.  A 224-column held
+      // tile stores its 112 columns per warp in 16-column chunks (the others
+      // in 64 or 32): its waves count 12% longer, as measured on GB300
+      // (4096^3 slow on pairs: 256 x 224 79.6 us against 256 x 256 75.4 us,
+      // both four waves).
+      constexpr double kHeld224Wave = 1.12;
       bn = 128;
       if (!mx && d.splitk <= 1 && tiles_r1 * cdiv(P->Q, 256) * L >= (int64_t)P->sms) {
         double best = 1e300;
         for (int c : {256, 224, 192}) {
           if (c != 256 && y_block128) continue;
           const int64_t tiles = tiles_r1 * cdiv(P->Q, c) * L;
-          const double cost = (double)cdiv(tiles, P->sms) * (kBlockM + c);
+          const double wide_cost = (kBlockM + c) * (c == 224 ? kHeld224Wave : 1.0);
+          const double cost = (double)cdiv(tiles, P->sms) * wide_cost;
           if (cost < best * 0.999) {
             best = cost;
             bn = c;
@@ -368,7 +374,7 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
           }
           if (d.cta_pair != 0) continue;
           const int64_t ptiles = pair_rows * cdiv(P->Q, c) * L;
-          const double pcost = (double)cdiv(ptiles, P->sms / 2) * (kBlockM + c) * kSlowPairWave;
+          const double pcost = (double)cdiv(ptiles, P->sms / 2) * wide_cost * kSlowPairWave;
           if (pcost < best * 0.999) {
             best = pcost;
             bn = c;

@@ -82,7 +82,7 @@ int main(void) {
     subprocess.run(["gcc", "-I" + os.path.join(ROOT, "include"), str(src), "-L" + libdir, "-lfp8mm",
                     "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
-    assert out[0].split()[1:] == ["224", "1", "1", "1"]  # held 256 x 224 pair tiles: four whole waves
+    assert out[0].split()[1:] == ["256", "1", "1", "1"]  # held 256 x 256 pair tiles
     assert "ALIGN" in out[1].upper()
 
 

@@ -37,18 +37,18 @@ def test_llm_4096_fast_uses_pair_tiles(lib):
     assert i["units"] == 16 * 19 and i["stages"] == 6 and i["grid"] == SMS
 
 
-def test_llm_4096_slow_uses_held_224_column_pair_tiles(lib):
-    # held pair tiles: 16 x 19 = 304 tiles of 256 x 224, exactly four waves over 76 SM pairs
+def test_llm_4096_slow_uses_held_256_column_pair_tiles(lib):
+    # held pair tiles of 256 x 256 (4 x 224-column waves cost more: their 112-column parts store
+    # in 16-column chunks)
     i = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0)
-    # 5 stages of 32 KiB beside the 56 KiB that stage a held tile's bf16 output
-    assert (i["cta_pair"], i["block_n"], i["splitk"], i["epi_warps"], i["slow"]) == (1, 224, 1, 8, 1)
-    assert i["stages"] == 5 and i["units"] == 16 * 19
-    # pairs off: one-CTA held tiles, 32 x 19 = 608 tiles of 128 x 224 (four waves over 152 SMs)
+    assert (i["cta_pair"], i["block_n"], i["splitk"], i["epi_warps"], i["slow"]) == (1, 256, 1, 8, 1)
+    assert i["stages"] == 5 and i["units"] == 16 * 16
+    # pairs off: one-CTA held tiles of 128 x 256
     j = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0, cta_pair=2)
-    assert (j["cta_pair"], j["block_n"], j["stages"], j["units"]) == (0, 224, 3, 32 * 19)
-    # fp32 outputs keep two 1 KiB chunk buffers per warp: one more stage
-    k = preview(4096, 4096, 4096, out_dtype=0, fast_accum=0)
-    assert (k["cta_pair"], k["block_n"], k["stages"]) == (1, 224, 6)
+    assert (j["cta_pair"], j["block_n"], j["units"]) == (0, 256, 32 * 16)
+    # on request: 256 x 224 pair tiles, 16 x 19 of them
+    k = preview(4096, 4096, 4096, out_dtype=1, fast_accum=0, block_n=224, cta_pair=1)
+    assert (k["cta_pair"], k["block_n"], k["units"]) == (1, 224, 16 * 19)
 
 
 @pytest.mark.parametrize("mode,stages", [(B.FP8MM_SCALE_A1x128_B128x128, 3), (B.FP8MM_SCALE_A1x128_B1x128, 2)])
