@@ -480,11 +480,14 @@ static fp8mm_status plan_impl(const fp8mm_desc* desc, int sms, int max_smem, boo
   P->splits = P->num_kb > 0 ? (int)cdiv(P->num_kb, P->kb_per_split) : 1;
   P->units = (long long)tiles * P->splits;
   P->grid = (int)std::min<long long>(P->units * P->cg, P->sms / P->cg * P->cg);
-  // Grouped raster: consecutive work units walk 8 tile rows of one tile column
-  // before moving to the next column, so a Y tile is read by 8 CTAs while it is
-  // in L2.  (Groups sized to keep all of X in L2 cut the DRAM re-reads of Y on
-  // the largest shapes 4-8x but measured 2-5% slower on GB300.)
-  P->group = swap ? 1 : 8;
+  // Grouped raster: consecutive work units walk a group of tile rows of one
+  // tile column before moving to the next column, so a Y tile is read by the
+  // group's CTAs while it is in L2: 8 one-CTA tile rows, 16 pair tile rows
+  // (4096 rows; on GB300 the pair shapes of 1024-8192 x 28672 x 8192 ran
+  // about 1% faster with 16 than with 8, 2-4% slower with 4 or 32).  (Groups
+  // sized to keep all of X in L2 cut the DRAM re-reads of Y on the largest
+  // shapes 4-8x but measured 2-5% slower.)
+  P->group = swap ? 1 : (P->cg == 2 ? 16 : 8);
 
   // Pipeline depth: as many stages as fit in shared memory (at most 12).  The
   // MX form also keeps a 16-column TMEM slot per stage for its factors, next
